@@ -1,1 +1,24 @@
-"""GB300-native block-sparse masked attention forward (Splash-style)."""
+"""GB300-native block-sparse masked attention forward (Splash-style).
+
+The compute runs in libbsm.so (hand-written CUDA for sm_103a) behind the C
+ABI of ``include/bsm.h``; this package is its Python binding.
+"""
+
+from .api import (  # noqa: F401
+    MASK_CAUSAL,
+    MASK_LOCAL,
+    MASK_SEGMENT,
+    SCORE_POINTWISE,
+    SCORE_SOFTMAX,
+    BsmError,
+    MaskInfo,
+    bsm_build_mask_info,
+    bsm_device_status,
+    bsm_last_error,
+    bsm_mask_info_bytes,
+    bsm_selftest_wait_timeout,
+    bsm_splash_fwd,
+    bsm_version,
+    build_mask_info,
+    splash_attention,
+)

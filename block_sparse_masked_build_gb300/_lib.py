@@ -1,0 +1,105 @@
+"""ctypes loader for libbsm.so (the C ABI of include/bsm.h).
+
+The library is loaded on first use.  There is no fallback: if the shared
+library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libbsm.so")
+
+BSM_OK = 0
+BSM_ERR_INVALID_ARG = -1
+BSM_ERR_UNSUPPORTED = -2
+BSM_ERR_CUDA = -3
+BSM_ERR_DEVICE_TIMEOUT = -4
+
+STATUS_NAMES = {
+    BSM_OK: "BSM_OK",
+    BSM_ERR_INVALID_ARG: "BSM_ERR_INVALID_ARG",
+    BSM_ERR_UNSUPPORTED: "BSM_ERR_UNSUPPORTED",
+    BSM_ERR_CUDA: "BSM_ERR_CUDA",
+    BSM_ERR_DEVICE_TIMEOUT: "BSM_ERR_DEVICE_TIMEOUT",
+}
+
+
+class MaskSpec(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("window", ctypes.c_int32)]
+
+
+class MaskInfoStruct(ctypes.Structure):
+    _fields_ = [
+        ("flags", ctypes.c_uint32),
+        ("window", ctypes.c_int32),
+        ("num_tables", ctypes.c_int32),
+        ("Sq", ctypes.c_int32),
+        ("Skv", ctypes.c_int32),
+        ("block_q", ctypes.c_int32),
+        ("block_kv", ctypes.c_int32),
+        ("nq", ctypes.c_int32),
+        ("nk", ctypes.c_int32),
+        ("block_mask", ctypes.c_void_p),
+        ("data_next", ctypes.c_void_p),
+        ("row_ptr", ctypes.c_void_p),
+        ("kv_idx", ctypes.c_void_p),
+        ("kv_cls", ctypes.c_void_p),
+    ]
+
+
+I64x3 = ctypes.c_int64 * 3
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    c = ctypes
+    lib.bsm_mask_info_bytes.restype = c.c_size_t
+    lib.bsm_mask_info_bytes.argtypes = [c.POINTER(MaskSpec), c.c_int32,
+                                        c.c_int32, c.c_int32, c.c_int32,
+                                        c.c_int32]
+    lib.bsm_build_mask_info.restype = c.c_int
+    lib.bsm_build_mask_info.argtypes = [
+        c.POINTER(MaskSpec), c.c_void_p, c.c_void_p, c.c_int32, c.c_int32,
+        c.c_int32, c.c_int32, c.c_int32, c.c_void_p, c.c_size_t,
+        c.POINTER(MaskInfoStruct), c.c_void_p]
+    lib.bsm_splash_fwd.restype = c.c_int
+    lib.bsm_splash_fwd.argtypes = [
+        c.c_void_p, c.c_void_p, c.c_void_p, I64x3, I64x3, I64x3, I64x3,
+        c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+        c.POINTER(MaskInfoStruct), c.c_void_p, c.c_void_p, c.c_float,
+        c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p]
+    lib.bsm_device_status.restype = c.c_int
+    lib.bsm_device_status.argtypes = [c.c_void_p, c.POINTER(c.c_int32)]
+    lib.bsm_selftest_wait_timeout.restype = c.c_int
+    lib.bsm_selftest_wait_timeout.argtypes = [c.c_int64, c.c_void_p]
+    lib.bsm_last_error.restype = c.c_char_p
+    lib.bsm_last_error.argtypes = []
+    lib.bsm_version.restype = c.c_int32
+    lib.bsm_version.argtypes = []
+    return lib
+
+
+def lib():
+    """The loaded library; raises if libbsm.so has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built: run "
+                    "`python -m block_sparse_masked_build_gb300.build` "
+                    "(there is no CPU fallback)")
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def last_error() -> str:
+    return lib().bsm_last_error().decode("utf-8", "replace")

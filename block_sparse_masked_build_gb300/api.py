@@ -1,0 +1,244 @@
+"""Python binding of the C ABI (same names as include/bsm.h) plus two thin
+conveniences that allocate with torch and call it.
+
+Every step of the computation runs in the CUDA kernels of libbsm.so; this
+module only marshals arguments (pointers, strides, the stream) and uses
+torch for device memory, pinned host memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import MaskInfoStruct, MaskSpec, I64x3
+
+MASK_CAUSAL = 1
+MASK_LOCAL = 2
+MASK_SEGMENT = 4
+SCORE_SOFTMAX = 0
+SCORE_POINTWISE = 1
+
+
+class BsmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = _lib.STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{name}: {message}")
+
+
+def _check(status: int) -> None:
+    if status != _lib.BSM_OK:
+        raise BsmError(status, _lib.last_error())
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+# --------------------------------------------------------------- C ABI names
+
+def bsm_version() -> int:
+    return int(_lib.lib().bsm_version())
+
+
+def bsm_last_error() -> str:
+    return _lib.last_error()
+
+
+def bsm_mask_info_bytes(flags: int, window: int, B: int, Sq: int, Skv: int,
+                        block_q: int, block_kv: int) -> int:
+    spec = MaskSpec(flags, window)
+    return int(_lib.lib().bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv,
+                                              block_q, block_kv))
+
+
+@dataclass
+class MaskInfo:
+    """Mask-info tables living in ``buffer`` (a CUDA uint8 tensor)."""
+
+    struct: MaskInfoStruct
+    buffer: torch.Tensor
+
+    def _view(self, ptr: int, dtype, count: int) -> torch.Tensor:
+        off = ptr - self.buffer.data_ptr()
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.buffer[off:off + nbytes].view(dtype)
+
+    @property
+    def num_tables(self) -> int:
+        return self.struct.num_tables
+
+    @property
+    def nq(self) -> int:
+        return self.struct.nq
+
+    @property
+    def nk(self) -> int:
+        return self.struct.nk
+
+    @property
+    def block_mask(self) -> torch.Tensor:
+        s = self.struct
+        return self._view(s.block_mask, torch.int8,
+                          s.num_tables * s.nq * s.nk).view(
+                              s.num_tables, s.nq, s.nk)
+
+    @property
+    def data_next(self) -> torch.Tensor:
+        s = self.struct
+        return self._view(s.data_next, torch.int32,
+                          s.num_tables * s.nq * s.nk).view(
+                              s.num_tables, s.nq, s.nk)
+
+    @property
+    def row_ptr(self) -> torch.Tensor:
+        s = self.struct
+        return self._view(s.row_ptr, torch.int32, s.num_tables * s.nq + 1)
+
+    def kv_lists(self) -> tuple[torch.Tensor, torch.Tensor]:
+        """(kv_idx, kv_cls) trimmed to row_ptr[-1] entries (synchronises)."""
+        s = self.struct
+        nnz = int(self.row_ptr[-1].item())
+        idx = self._view(s.kv_idx, torch.int32, s.num_tables * s.nq * s.nk)
+        cls = self._view(s.kv_cls, torch.int8, s.num_tables * s.nq * s.nk)
+        return idx[:nnz], cls[:nnz]
+
+
+def bsm_build_mask_info(flags: int, window: int, q_segment_ids, kv_segment_ids,
+                        B: int, Sq: int, Skv: int, block_q: int, block_kv: int,
+                        buffer: torch.Tensor, stream=None) -> MaskInfo:
+    spec = MaskSpec(flags, window)
+    info = MaskInfoStruct()
+    _check(_lib.lib().bsm_build_mask_info(
+        ctypes.byref(spec), _ptr(q_segment_ids), _ptr(kv_segment_ids), B, Sq,
+        Skv, block_q, block_kv, buffer.data_ptr(),
+        buffer.numel() * buffer.element_size(), ctypes.byref(info),
+        _stream_handle(stream)))
+    return MaskInfo(info, buffer)
+
+
+def _strides3(t: torch.Tensor):
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("tensors must be 4-D [B, H, S, D] views with a "
+                         "contiguous head dimension")
+    return I64x3(t.stride(0), t.stride(1), t.stride(2))
+
+
+def bsm_splash_fwd(q, k, v, mask_info: MaskInfo, q_segment_ids,
+                   kv_segment_ids, scale: float, score: int, out,
+                   lse=None, stream=None) -> None:
+    """q [B,H,Sq,D], k/v [B,H_kv,Skv,D], out [B,H,Sq,D] (bf16, CUDA)."""
+    B, H, Sq, D = q.shape
+    H_kv, Skv = k.shape[1], k.shape[2]
+    _check(_lib.lib().bsm_splash_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides3(q), _strides3(k),
+        _strides3(v), _strides3(out), B, H, H_kv, Sq, Skv, D,
+        ctypes.byref(mask_info.struct), _ptr(q_segment_ids),
+        _ptr(kv_segment_ids), float(scale), int(score), out.data_ptr(),
+        _ptr(lse), _stream_handle(stream)))
+
+
+def bsm_device_status(stream=None) -> tuple[int, list[int]]:
+    detail = (ctypes.c_int32 * 4)()
+    st = _lib.lib().bsm_device_status(_stream_handle(stream), detail)
+    return int(st), list(detail)
+
+
+def bsm_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(_lib.lib().bsm_selftest_wait_timeout(int(timeout_ns),
+                                                _stream_handle(stream)))
+
+
+# ------------------------------------------------------------ conveniences
+
+def build_mask_info(flags: int, B: int, Sq: int, Skv: int, block_q: int = 128,
+                    block_kv: int = 128, window: int = 0, q_segment_ids=None,
+                    kv_segment_ids=None, device=None, stream=None) -> MaskInfo:
+    """Allocate the mask-info buffer with torch and build the tables."""
+    nbytes = bsm_mask_info_bytes(flags, window, B, Sq, Skv, block_q, block_kv)
+    if nbytes == 0:
+        raise BsmError(_lib.BSM_ERR_INVALID_ARG, bsm_last_error())
+    if device is None:
+        device = (q_segment_ids.device if q_segment_ids is not None
+                  else torch.device("cuda"))
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return bsm_build_mask_info(flags, window, q_segment_ids, kv_segment_ids, B,
+                               Sq, Skv, block_q, block_kv, buf, stream)
+
+
+def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
+                     window: int = 0, q_segment_ids=None, kv_segment_ids=None,
+                     scale: float | None = None, score: int = SCORE_SOFTMAX,
+                     block_q: int = 128, block_kv: int = 128,
+                     mask_info: MaskInfo | None = None,
+                     return_lse: bool = True, out=None, lse=None,
+                     stream=None):
+    """Block-sparse masked attention forward, q/k/v [B, H, S, D] bf16.
+
+    Defaults follow hstu_ops ``pointwise_splash_attention``: scale =
+    1/sqrt(D).  With CUDA inputs everything stays on the device.  With CPU
+    inputs (ideally pinned) the inputs are copied to the current device,
+    the kernels run there, and ``out``/``lse`` are copied back into host
+    tensors (``out``/``lse`` may be given, pinned, to be reused).
+    Returns (out, lse); lse is None for the pointwise path or when
+    ``return_lse`` is False.
+    """
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    host = q.device.type == "cpu"
+    dev = torch.device("cuda", torch.cuda.current_device()) if host \
+        else q.device
+    want_lse = return_lse and score == SCORE_SOFTMAX
+    if host:
+        nb = q.is_pinned()
+        qd = q.to(dev, non_blocking=nb)
+        kd = k.to(dev, non_blocking=nb)
+        vd = v.to(dev, non_blocking=nb)
+        qs = None if q_segment_ids is None else \
+            q_segment_ids.to(dev, non_blocking=nb)
+        ks = None if kv_segment_ids is None else \
+            kv_segment_ids.to(dev, non_blocking=nb)
+    else:
+        qd, kd, vd, qs, ks = q, k, v, q_segment_ids, kv_segment_ids
+    if mask_info is None:
+        mask_info = build_mask_info(mask_flags, B, Sq, Skv, block_q, block_kv,
+                                    window, qs, ks, device=dev, stream=stream)
+    od = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=dev) \
+        if (host or out is None) else out
+    ld = None
+    if want_lse:
+        ld = torch.empty((B, H, Sq), dtype=torch.float32, device=dev) \
+            if (host or lse is None) else lse
+    bsm_splash_fwd(qd, kd, vd, mask_info, qs, ks, scale, score, od, ld,
+                   stream)
+    if not host:
+        return od, ld
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16,
+                          pin_memory=True)
+    out.copy_(od, non_blocking=True)
+    if want_lse:
+        if lse is None:
+            lse = torch.empty((B, H, Sq), dtype=torch.float32,
+                              pin_memory=True)
+        lse.copy_(ld, non_blocking=True)
+    if stream is None:
+        torch.cuda.current_stream(dev).synchronize()
+    else:
+        stream.synchronize()
+    return out, (lse if want_lse else None)

@@ -1,0 +1,396 @@
+// Host side of the C ABI declared in include/bsm.h: argument validation,
+// layout of the caller's mask-info buffer, TMA tensor-map encoding and the
+// kernel launches.  Allocates no device memory.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "bsm_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+bsm_status fail(bsm_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+bsm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(BSM_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                  cudaGetErrorString(e) + ")");
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool is_block_size(int32_t b) {
+  return b >= 16 && b <= 512 && (b & (b - 1)) == 0;
+}
+
+struct MiLayout {
+  size_t off_bm, off_dn, off_rp, off_idx, off_cls, total;
+};
+
+MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk) {
+  const size_t cells = static_cast<size_t>(tables * nq * nk);
+  const size_t rows = static_cast<size_t>(tables * nq);
+  MiLayout L;
+  size_t o = 0;
+  L.off_bm = o;
+  o = align_up(o + cells, 256);
+  L.off_dn = o;
+  o = align_up(o + cells * 4, 256);
+  L.off_rp = o;
+  o = align_up(o + (rows + 1) * 4, 256);
+  L.off_idx = o;
+  o = align_up(o + cells * 4, 256);
+  L.off_cls = o;
+  o = align_up(o + cells, 256);
+  L.total = o;
+  return L;
+}
+
+bsm_status check_spec(const bsm_mask_spec* spec) {
+  if (spec == nullptr) return fail(BSM_ERR_INVALID_ARG, "mask spec is NULL");
+  const uint32_t known = BSM_MASK_CAUSAL | BSM_MASK_LOCAL | BSM_MASK_SEGMENT;
+  if (spec->flags & ~known)
+    return fail(BSM_ERR_INVALID_ARG, "unknown mask flag bits");
+  if ((spec->flags & BSM_MASK_LOCAL) && spec->window < 1)
+    return fail(BSM_ERR_INVALID_ARG, "local window must be >= 1");
+  return BSM_OK;
+}
+
+bsm_status check_mi_shape(const bsm_mask_spec* spec, int32_t B, int32_t Sq,
+                          int32_t Skv, int32_t bq, int32_t bkv) {
+  bsm_status s = check_spec(spec);
+  if (s != BSM_OK) return s;
+  if (B < 0 || Sq < 0 || Skv < 0)
+    return fail(BSM_ERR_INVALID_ARG, "negative size");
+  if (Sq > bsm::kMaxSeq || Skv > bsm::kMaxSeq)
+    return fail(BSM_ERR_UNSUPPORTED, "sequence length above 262144");
+  if (!is_block_size(bq) || !is_block_size(bkv))
+    return fail(BSM_ERR_INVALID_ARG,
+                "block_q and block_kv must be powers of two in [16, 512]");
+  return BSM_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 map over [B][H][S][D] storage with element strides (sb, sh, ss);
+// box = 64 head-dim elements (128 bytes, 128-byte swizzle) x 128 rows.
+bsm_status make_map(CUtensorMap* map, const void* ptr, int32_t B, int32_t H,
+                    int32_t S, int32_t D, const int64_t strides[3],
+                    const char* name) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr)
+    return fail(BSM_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  // Strides of size-1 dimensions are never used; give them a valid value.
+  const int64_t ss = S > 1 ? strides[2] : D;
+  const int64_t sh = H > 1 ? strides[1] : ss * S;
+  const int64_t sb = B > 1 ? strides[0] : sh * H;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t gstr[3] = {static_cast<cuuint64_t>(ss * 2),
+                        static_cast<cuuint64_t>(sh * 2),
+                        static_cast<cuuint64_t>(sb * 2)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(bsm::kTileM), 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(ptr), dims, gstr, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(BSM_ERR_INVALID_ARG,
+                std::string("tensor map for ") + name +
+                    " rejected (strides must be multiples of 8 elements)");
+  return BSM_OK;
+}
+
+bsm_status check_device(int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3)
+    return fail(BSM_ERR_UNSUPPORTED,
+                "libbsm is built for sm_103a (GB300) only; device is sm_" +
+                    std::to_string(major) + std::to_string(minor));
+  if (num_sms) *num_sms = sms;
+  return BSM_OK;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("BSM_WAIT_TIMEOUT_NS");
+    if (s != nullptr) {
+      const unsigned long long x = std::strtoull(s, nullptr, 10);
+      if (x >= 1000ull && x <= 100000000000ull) return static_cast<uint64_t>(x);
+    }
+    return static_cast<uint64_t>(2000000000ull);  // 2 s
+  }();
+  return v;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bsm_mask_info_bytes(const bsm_mask_spec* spec, int32_t B, int32_t Sq,
+                           int32_t Skv, int32_t block_q, int32_t block_kv) {
+  if (check_mi_shape(spec, B, Sq, Skv, block_q, block_kv) != BSM_OK) return 0;
+  const int64_t tables = (spec->flags & BSM_MASK_SEGMENT) ? B : 1;
+  const int64_t nq = (Sq + block_q - 1) / block_q;
+  const int64_t nk = (Skv + block_kv - 1) / block_kv;
+  return mi_layout(tables, nq, nk).total;
+}
+
+bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
+                               const int32_t* q_segment_ids,
+                               const int32_t* kv_segment_ids, int32_t B,
+                               int32_t Sq, int32_t Skv, int32_t block_q,
+                               int32_t block_kv, void* buffer,
+                               size_t buffer_bytes, bsm_mask_info* info,
+                               void* stream) {
+  g_last_error.clear();
+  bsm_status s = check_mi_shape(spec, B, Sq, Skv, block_q, block_kv);
+  if (s != BSM_OK) return s;
+  if (info == nullptr) return fail(BSM_ERR_INVALID_ARG, "info is NULL");
+  const bool seg = (spec->flags & BSM_MASK_SEGMENT) != 0;
+  if (seg && (q_segment_ids == nullptr || kv_segment_ids == nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "BSM_MASK_SEGMENT needs both q and kv segment ids");
+  if (!seg && (q_segment_ids != nullptr || kv_segment_ids != nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "segment ids given without BSM_MASK_SEGMENT");
+  if (seg && B < 1) return fail(BSM_ERR_INVALID_ARG, "B must be >= 1");
+  const int64_t tables = seg ? B : 1;
+  const int64_t nq = (Sq + block_q - 1) / block_q;
+  const int64_t nk = (Skv + block_kv - 1) / block_kv;
+  if (tables > 65535)
+    return fail(BSM_ERR_UNSUPPORTED, "too many mask tables");
+  const MiLayout L = mi_layout(tables, nq, nk);
+  if (buffer == nullptr) return fail(BSM_ERR_INVALID_ARG, "buffer is NULL");
+  if ((reinterpret_cast<uintptr_t>(buffer) & 255u) != 0)
+    return fail(BSM_ERR_INVALID_ARG, "buffer must be 256-byte aligned");
+  if (buffer_bytes < L.total)
+    return fail(BSM_ERR_INVALID_ARG,
+                "buffer too small: need " + std::to_string(L.total) +
+                    " bytes");
+  s = check_device(nullptr);
+  if (s != BSM_OK) return s;
+
+  uint8_t* base = static_cast<uint8_t*>(buffer);
+  bsm_mask_info mi;
+  mi.flags = spec->flags;
+  mi.window = (spec->flags & BSM_MASK_LOCAL) ? spec->window : 0;
+  mi.num_tables = static_cast<int32_t>(tables);
+  mi.Sq = Sq;
+  mi.Skv = Skv;
+  mi.block_q = block_q;
+  mi.block_kv = block_kv;
+  mi.nq = static_cast<int32_t>(nq);
+  mi.nk = static_cast<int32_t>(nk);
+  mi.block_mask = reinterpret_cast<int8_t*>(base + L.off_bm);
+  mi.data_next = reinterpret_cast<int32_t*>(base + L.off_dn);
+  mi.row_ptr = reinterpret_cast<int32_t*>(base + L.off_rp);
+  mi.kv_idx = reinterpret_cast<int32_t*>(base + L.off_idx);
+  mi.kv_cls = reinterpret_cast<int8_t*>(base + L.off_cls);
+
+  bsm::MaskInfoParams p;
+  p.flags = mi.flags;
+  p.window = mi.window;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.bq = block_q;
+  p.bkv = block_kv;
+  p.nq = mi.nq;
+  p.nk = mi.nk;
+  p.tables = mi.num_tables;
+  p.q_seg = q_segment_ids;
+  p.kv_seg = kv_segment_ids;
+  p.block_mask = mi.block_mask;
+  p.data_next = mi.data_next;
+  p.row_ptr = mi.row_ptr;
+  p.kv_idx = mi.kv_idx;
+  p.kv_cls = mi.kv_cls;
+  cudaError_t e =
+      bsm::launch_mask_info(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mask-info launch");
+  *info = mi;
+  return BSM_OK;
+}
+
+bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
+                          const int64_t q_strides[3],
+                          const int64_t k_strides[3],
+                          const int64_t v_strides[3],
+                          const int64_t o_strides[3], int32_t B, int32_t H,
+                          int32_t H_kv, int32_t Sq, int32_t Skv, int32_t D,
+                          const bsm_mask_info* info,
+                          const int32_t* q_segment_ids,
+                          const int32_t* kv_segment_ids, float scale,
+                          int32_t score, void* out, float* lse, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || H < 0 || H_kv < 0 || Sq < 0 || Skv < 0)
+    return fail(BSM_ERR_INVALID_ARG, "negative size");
+  if (H_kv == 0 ? H != 0 : (H % H_kv) != 0)
+    return fail(BSM_ERR_INVALID_ARG, "H must be a multiple of H_kv");
+  if (D != 64 && D != 128)
+    return fail(BSM_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (Sq > bsm::kMaxSeq || Skv > bsm::kMaxSeq)
+    return fail(BSM_ERR_UNSUPPORTED, "sequence length above 262144");
+  if (score != BSM_SCORE_SOFTMAX && score != BSM_SCORE_POINTWISE)
+    return fail(BSM_ERR_INVALID_ARG, "unknown score path");
+  if (score == BSM_SCORE_POINTWISE && lse != nullptr)
+    return fail(BSM_ERR_INVALID_ARG,
+                "the pointwise score path has no logsumexp; pass lse = NULL");
+  if (!std::isfinite(scale)) return fail(BSM_ERR_INVALID_ARG, "scale not finite");
+  if (info == nullptr) return fail(BSM_ERR_INVALID_ARG, "mask info is NULL");
+  if (info->Sq != Sq || info->Skv != Skv)
+    return fail(BSM_ERR_INVALID_ARG,
+                "mask info was built for other sequence lengths");
+  const bool seg = (info->flags & BSM_MASK_SEGMENT) != 0;
+  if (info->num_tables != (seg ? B : 1))
+    return fail(BSM_ERR_INVALID_ARG,
+                "mask info was built for another batch size");
+  if (!is_block_size(info->block_q) || !is_block_size(info->block_kv) ||
+      info->nq != (Sq + info->block_q - 1) / info->block_q ||
+      info->nk != (Skv + info->block_kv - 1) / info->block_kv)
+    return fail(BSM_ERR_INVALID_ARG, "inconsistent mask info");
+  if (seg && (q_segment_ids == nullptr || kv_segment_ids == nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "BSM_MASK_SEGMENT needs both q and kv segment ids");
+  if (!seg && (q_segment_ids != nullptr || kv_segment_ids != nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "segment ids given without BSM_MASK_SEGMENT");
+  const int64_t n_super = (Sq + bsm::kUnitRows - 1) / bsm::kUnitRows;
+  const int64_t units = static_cast<int64_t>(B) * H * n_super;
+  if (units == 0) return BSM_OK;
+  if (units > 0x7fffffff) return fail(BSM_ERR_UNSUPPORTED, "too many tiles");
+  if (q == nullptr || out == nullptr || (Skv > 0 && (k == nullptr || v == nullptr)))
+    return fail(BSM_ERR_INVALID_ARG, "NULL tensor");
+  if (q_strides == nullptr || k_strides == nullptr || v_strides == nullptr ||
+      o_strides == nullptr)
+    return fail(BSM_ERR_INVALID_ARG, "NULL strides");
+  if (!aligned16(q) || !aligned16(out) || (Skv > 0 && (!aligned16(k) || !aligned16(v))))
+    return fail(BSM_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const int64_t sizes_q[3] = {B, H, Sq};
+  const int64_t sizes_kv[3] = {B, H_kv, Skv};
+  for (int d = 0; d < 3; ++d) {
+    if (sizes_q[d] > 1 && ((q_strides[d] % 8) != 0 || q_strides[d] <= 0))
+      return fail(BSM_ERR_INVALID_ARG, "q strides must be positive multiples of 8");
+    if (sizes_q[d] > 1 && ((o_strides[d] % 8) != 0 || o_strides[d] <= 0))
+      return fail(BSM_ERR_INVALID_ARG, "out strides must be positive multiples of 8");
+    if (Skv > 0 && sizes_kv[d] > 1 && ((k_strides[d] % 8) != 0 || k_strides[d] <= 0 ||
+                            (v_strides[d] % 8) != 0 || v_strides[d] <= 0))
+      return fail(BSM_ERR_INVALID_ARG, "k/v strides must be positive multiples of 8");
+  }
+  int num_sms = 0;
+  bsm_status s = check_device(&num_sms);
+  if (s != BSM_OK) return s;
+
+  CUtensorMap tq, tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  s = make_map(&tq, q, B, H, Sq, D, q_strides, "q");
+  if (s != BSM_OK) return s;
+  if (Skv > 0) {
+    s = make_map(&tk, k, B, H_kv, Skv, D, k_strides, "k");
+    if (s != BSM_OK) return s;
+    s = make_map(&tv, v, B, H_kv, Skv, D, v_strides, "v");
+    if (s != BSM_OK) return s;
+  }
+
+  bsm::FwdParams p;
+  p.B = B;
+  p.H = H;
+  p.Hkv = H_kv;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.D = D;
+  p.n_super = static_cast<int32_t>(n_super);
+  p.n_kvtiles = (Skv + bsm::kTileN - 1) / bsm::kTileN;
+  p.num_units = static_cast<int32_t>(units);
+  p.flags = info->flags;
+  p.window = info->window;
+  p.block_mask = info->block_mask;
+  p.mi_nq = info->nq;
+  p.mi_nk = info->nk;
+  p.bq = info->block_q;
+  p.bkv = info->block_kv;
+  p.tables = info->num_tables;
+  p.q_seg = q_segment_ids;
+  p.kv_seg = kv_segment_ids;
+  p.score = score;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale = scale;
+  p.inv_sq = Sq > 0 ? static_cast<float>(1.0 / static_cast<double>(Sq)) : 0.f;
+  p.out = static_cast<uint16_t*>(out);
+  p.o_sb = o_strides[0];
+  p.o_sh = o_strides[1];
+  p.o_ss = o_strides[2];
+  p.lse = lse;
+  p.timeout_ns = wait_timeout_ns();
+  cudaError_t e = bsm::launch_splash_fwd(p, tq, tk, tv, num_sms,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "splash_fwd launch");
+  return BSM_OK;
+}
+
+bsm_status bsm_device_status(void* stream, int32_t* detail) {
+  g_last_error.clear();
+  int32_t rec[4] = {0, 0, 0, 0};
+  cudaError_t e = bsm::read_device_error(rec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "device status");
+  if (detail != nullptr) std::memcpy(detail, rec, sizeof(rec));
+  if (rec[0] != 0)
+    return fail(BSM_ERR_DEVICE_TIMEOUT,
+                "a kernel gave up on a bounded wait (block " +
+                    std::to_string(rec[1]) + ", role " + std::to_string(rec[2]) +
+                    ", phase " + std::to_string(rec[3]) + ")");
+  return BSM_OK;
+}
+
+bsm_status bsm_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
+  g_last_error.clear();
+  if (timeout_ns < 1000 || timeout_ns > 10000000000LL)
+    return fail(BSM_ERR_INVALID_ARG, "timeout_ns must be in [1e3, 1e10]");
+  bsm_status s = check_device(nullptr);
+  if (s != BSM_OK) return s;
+  cudaError_t e = bsm::launch_wait_selftest(static_cast<uint64_t>(timeout_ns),
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return BSM_OK;
+}
+
+const char* bsm_last_error(void) { return g_last_error.c_str(); }
+
+int32_t bsm_version(void) { return 100; }
+
+}  // extern "C"

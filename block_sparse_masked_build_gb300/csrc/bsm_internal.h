@@ -1,0 +1,68 @@
+// Internal declarations shared by the host C ABI (bsm_api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/bsm.h"
+
+namespace bsm {
+
+// Query tile (rows of one tcgen05 accumulator) and KV tile of the forward
+// kernel; one work unit is two query tiles (256 rows) of one (batch, head).
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kUnitRows = 2 * kTileM;
+constexpr int kMaxSeq = 262144;
+constexpr int kMaxKvTiles = kMaxSeq / kTileN;  // list capacity per unit
+
+struct MaskInfoParams {
+  uint32_t flags;
+  int32_t window;
+  int32_t Sq, Skv, bq, bkv, nq, nk, tables;
+  const int32_t* q_seg;   // [tables][Sq] (SEGMENT only)
+  const int32_t* kv_seg;  // [tables][Skv]
+  int8_t* block_mask;
+  int32_t* data_next;
+  int32_t* row_ptr;
+  int32_t* kv_idx;
+  int8_t* kv_cls;
+};
+
+struct FwdParams {
+  int32_t B, H, Hkv, Sq, Skv, D;
+  int32_t n_super;    // ceil(Sq / 256)
+  int32_t n_kvtiles;  // ceil(Skv / 128)
+  int32_t num_units;  // B * H * n_super
+  // mask
+  uint32_t flags;
+  int32_t window;
+  const int8_t* block_mask;  // [tables][mi_nq][mi_nk]
+  int32_t mi_nq, mi_nk, bq, bkv, tables;
+  const int32_t* q_seg;   // [B][Sq]
+  const int32_t* kv_seg;  // [B][Skv]
+  // scores
+  int32_t score;     // bsm_score
+  float scale_log2;  // softmax: scale * log2(e)
+  float scale;       // pointwise
+  float inv_sq;      // pointwise: 1 / Sq
+  // outputs
+  uint16_t* out;  // bf16 bits
+  int64_t o_sb, o_sh, o_ss;
+  float* lse;
+  uint64_t timeout_ns;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream);
+cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+// Reads and clears the device error record of the forward kernel TU.
+cudaError_t read_device_error(int32_t out[4], cudaStream_t stream);
+
+}  // namespace bsm

@@ -1,0 +1,268 @@
+// Device mask-info builder.
+//
+// Classifies every (q-block, kv-block) of the mask as empty (0), partial (1)
+// or full (2) -- the encoding of hstu_ops `_next_nonzero` -- and emits the
+// next-block table (splash notes section 21: an empty step points at the
+// next nonzero block) plus per-row CSR lists of the nonzero blocks.
+//
+// Three launches:
+//   1. classify: one CTA per (table, q-block row).  Causal/local blocks are
+//      classified exactly from the range of q - k over the block; blocks
+//      that also carry a segment mask are decided from the min/max of the
+//      segment ids when that settles it, else by scanning every element.
+//      Writes block_mask, data_next and the row's nonzero count.
+//   2. scan: one CTA turns the counts into CSR row offsets.
+//   3. compact: one CTA per row writes the ascending nonzero list.
+#include <cstdint>
+
+#include "bsm_internal.h"
+
+namespace bsm {
+namespace {
+
+constexpr int kMiThreads = 256;
+constexpr int kNegInf = -(1 << 30);
+constexpr int kPosInf = (1 << 30);
+
+struct BlockRange {
+  int r0, r1, c0, c1;  // inclusive, clipped to the sequence
+  bool ragged;
+};
+
+__device__ __forceinline__ BlockRange block_range(const MaskInfoParams& p,
+                                                  int i, int j) {
+  BlockRange br;
+  br.r0 = i * p.bq;
+  br.r1 = min(p.Sq, br.r0 + p.bq) - 1;
+  br.c0 = j * p.bkv;
+  br.c1 = min(p.Skv, br.c0 + p.bkv) - 1;
+  br.ragged = (br.r1 - br.r0 + 1 != p.bq) || (br.c1 - br.c0 + 1 != p.bkv);
+  return br;
+}
+
+// Causal/local part: every integer d = q - k in [r0 - c1, r1 - c0] occurs in
+// the (clipped) block; the allowed set is [lo, hi].
+__device__ __forceinline__ int base_class(const MaskInfoParams& p,
+                                          const BlockRange& br) {
+  const int lo = (p.flags & BSM_MASK_CAUSAL) ? 0 : kNegInf;
+  const int hi = (p.flags & BSM_MASK_LOCAL) ? p.window - 1 : kPosInf;
+  const int dmin = br.r0 - br.c1, dmax = br.r1 - br.c0;
+  if (dmax < lo || dmin > hi) return 0;
+  return (dmin >= lo && dmax <= hi && !br.ragged) ? 2 : 1;
+}
+
+__device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
+                                             int k) {
+  bool v = true;
+  if (p.flags & BSM_MASK_CAUSAL) v = v && (k <= q);
+  if (p.flags & BSM_MASK_LOCAL) v = v && (q - k < p.window);
+  return v;
+}
+
+__global__ void __launch_bounds__(kMiThreads)
+    mi_classify_kernel(const MaskInfoParams p) {
+  extern __shared__ int8_t cls_s[];  // [nk]
+  __shared__ int qseg_s[512];
+  __shared__ int red_min[kMiThreads / 32], red_max[kMiThreads / 32];
+  __shared__ int cnt_s;
+
+  const int i = blockIdx.x, t = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
+  const int r0 = i * p.bq, r1 = min(p.Sq, r0 + p.bq) - 1;
+
+  int qmin = kPosInf, qmax = kNegInf;
+  if (seg) {
+    const int32_t* qs = p.q_seg + static_cast<int64_t>(t) * p.Sq;
+    for (int r = r0 + threadIdx.x; r <= r1; r += blockDim.x) {
+      const int v = qs[r];
+      qseg_s[r - r0] = v;
+      qmin = min(qmin, v);
+      qmax = max(qmax, v);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      qmin = min(qmin, __shfl_xor_sync(0xffffffffu, qmin, o));
+      qmax = max(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+    }
+    if (lane == 0) {
+      red_min[warp] = qmin;
+      red_max[warp] = qmax;
+    }
+  }
+  if (threadIdx.x == 0) cnt_s = 0;
+  __syncthreads();
+  if (seg) {
+    qmin = red_min[0];
+    qmax = red_max[0];
+    for (int w = 1; w < kMiThreads / 32; ++w) {
+      qmin = min(qmin, red_min[w]);
+      qmax = max(qmax, red_max[w]);
+    }
+  }
+
+  // One warp per block (i, j).
+  int my_count = 0;
+  for (int j = warp; j < p.nk; j += kMiThreads / 32) {
+    const BlockRange br = block_range(p, i, j);
+    int c = base_class(p, br);
+    if (seg && c != 0) {
+      const int32_t* ks = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
+      int kmin = kPosInf, kmax = kNegInf;
+      for (int k = br.c0 + lane; k <= br.c1; k += 32) {
+        const int v = ks[k];
+        kmin = min(kmin, v);
+        kmax = max(kmax, v);
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      }
+      if (qmax < kmin || qmin > kmax) {
+        c = 0;  // no id occurs on both sides
+      } else if (qmin == qmax && kmin == kmax) {
+        // one segment covers the whole block: the causal/local class stands
+      } else {
+        // exact element scan; columns past Skv and rows past Sq are
+        // invisible, so a ragged block is never full
+        bool any = false, all = !br.ragged;
+        for (int cb = 0; cb < p.bkv; cb += 32) {
+          const int k = br.c0 + cb + lane;
+          const bool kin = (cb + lane < p.bkv) && (k <= br.c1);
+          const int kv = kin ? ks[k] : 0;
+          for (int r = br.r0; r <= br.r1; ++r) {
+            const bool v = kin && base_visible(p, r, k) && qseg_s[r - br.r0] == kv;
+            any |= v;
+            all &= v || (cb + lane >= p.bkv);
+          }
+          const bool wany = __any_sync(0xffffffffu, any);
+          const bool wall = __all_sync(0xffffffffu, all);
+          if (wany && !wall) break;  // already known to be partial
+        }
+        any = __any_sync(0xffffffffu, any);
+        all = __all_sync(0xffffffffu, all);
+        c = any ? (all ? 2 : 1) : 0;
+      }
+    }
+    if (lane == 0) {
+      cls_s[j] = static_cast<int8_t>(c);
+      my_count += (c != 0);
+    }
+  }
+  if (lane == 0 && my_count) atomicAdd(&cnt_s, my_count);
+  __syncthreads();
+
+  const int64_t row = static_cast<int64_t>(t) * p.nq + i;
+  int8_t* bm = p.block_mask + row * p.nk;
+  for (int j = threadIdx.x; j < p.nk; j += blockDim.x) bm[j] = cls_s[j];
+  if (threadIdx.x == 0) p.row_ptr[row + 1] = cnt_s;
+
+  // Next-block table, warp 0, right to left in chunks of 32.
+  if (warp == 0) {
+    int32_t* dn = p.data_next + row * p.nk;
+    const int nchunks = (p.nk + 31) / 32;
+    int last_nz = -1;
+    for (int ch = nchunks - 1; ch >= 0 && last_nz < 0; --ch) {
+      const int j = ch * 32 + lane;
+      const unsigned m = __ballot_sync(0xffffffffu, j < p.nk && cls_s[j] != 0);
+      if (m) last_nz = ch * 32 + 31 - __clz(m);
+    }
+    int carry = -1;  // nearest nonzero to the right of the current chunk
+    for (int ch = nchunks - 1; ch >= 0; --ch) {
+      const int j = ch * 32 + lane;
+      const unsigned m = __ballot_sync(0xffffffffu, j < p.nk && cls_s[j] != 0);
+      const unsigned hi = m & (0xffffffffu << lane);
+      int nxt = hi ? ch * 32 + __ffs(hi) - 1 : carry;
+      if (nxt < 0) nxt = last_nz < 0 ? 0 : last_nz;
+      if (j < p.nk) dn[j] = nxt;
+      if (m) carry = ch * 32 + __ffs(m) - 1;
+    }
+  }
+}
+
+// Inclusive scan of row_ptr[1..R] in place (row_ptr[0] = 0): CSR offsets.
+__global__ void __launch_bounds__(1024) mi_scan_kernel(int32_t* row_ptr,
+                                                       int R) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry_s;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    row_ptr[0] = 0;
+    carry_s = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int idx = base + threadIdx.x;
+    int v = idx < R ? row_ptr[idx + 1] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int s = warp_sums[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += n;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int carry = carry_s;
+    const int prefix = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (idx < R) row_ptr[idx + 1] = v + prefix;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry_s = carry + warp_sums[31];
+    __syncthreads();
+  }
+}
+
+// Ascending list of the nonzero blocks of one row.
+__global__ void __launch_bounds__(kMiThreads)
+    mi_compact_kernel(const MaskInfoParams p) {
+  __shared__ int warp_cnt[kMiThreads / 32];
+  const int i = blockIdx.x, t = blockIdx.y;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int64_t row = static_cast<int64_t>(t) * p.nq + i;
+  const int8_t* bm = p.block_mask + row * p.nk;
+  int base = p.row_ptr[row];
+  for (int j0 = 0; j0 < p.nk; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    const int8_t c = j < p.nk ? bm[j] : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kMiThreads / 32; ++w) {
+      before += (w < warp) ? warp_cnt[w] : 0;
+      total += warp_cnt[w];
+    }
+    if (c != 0) {
+      const int pos = base + before + __popc(m & ((1u << lane) - 1u));
+      p.kv_idx[pos] = j;
+      p.kv_cls[pos] = c;
+    }
+    base += total;
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
+  const int R = p.tables * p.nq;
+  if (R == 0) {
+    return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t), stream);
+  }
+  const size_t smem = static_cast<size_t>(p.nk > 0 ? p.nk : 1);
+  mi_classify_kernel<<<dim3(p.nq, p.tables), kMiThreads, smem, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mi_scan_kernel<<<1, 1024, 0, stream>>>(p.row_ptr, R);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bsm

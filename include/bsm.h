@@ -1,0 +1,175 @@
+/*
+ * bsm.h -- block-sparse masked attention forward (Splash-style) on GB300.
+ *
+ * C ABI of libbsm.so.  All compute runs in hand-written CUDA kernels for
+ * sm_103a; there is no CPU path.  The library allocates no device memory:
+ * the caller owns every buffer (inputs, outputs and the mask-info buffer).
+ * Pointers marked "device" must be device (or managed) memory of the current
+ * CUDA device; `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Work is enqueued asynchronously; argument errors are
+ * returned synchronously, before anything is enqueued, with a message in
+ * bsm_last_error().  No function falls back to another algorithm silently.
+ *
+ * Sources (page title, section):
+ *   [HSTU]   RecML "recml/core/ops/hstu_ops.py" -- pointwise splash attention:
+ *            _next_nonzero (block classes), _apply_mask (element mask),
+ *            _pointwise_splash_attention_fwd_kernel_impl (pointwise scores),
+ *            pointwise_splash_attention (API, defaults, argument checks).
+ *   [NOTES]  "JAX 到 VLIW, Pallas / Splash Attention 复习笔记" -- section 12
+ *            (naive attention), 15 (online softmax m/l/o), 18-19 (grid
+ *            h, i, j), 21 (sparse K/V indirection via data_next).
+ *   [KERNELS] "Attention Kernels -- Splash, Flash, SDPA on TPU" -- section
+ *            "Splash Attention via call_jax" (make_splash_mha(mask) then
+ *            kernel(q, k, v)).
+ */
+#ifndef BSM_H_
+#define BSM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsm_status {
+  BSM_OK = 0,
+  BSM_ERR_INVALID_ARG = -1,    /* bad shape, pointer, stride or size */
+  BSM_ERR_UNSUPPORTED = -2,    /* valid but not built (e.g. head_dim 96) */
+  BSM_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed */
+  BSM_ERR_DEVICE_TIMEOUT = -4  /* a kernel gave up waiting (see below) */
+} bsm_status;
+
+/* Score path.  SOFTMAX: out = softmax(scale * q k^T restricted to the
+ * visible keys) v, plus the per-row logsumexp ([NOTES] section 15).
+ * POINTWISE: out = sum over visible keys of x*sigmoid(x)/Sq * v with
+ * x = scale * q.k, no normalisation ([HSTU] fwd kernel impl). */
+typedef enum bsm_score {
+  BSM_SCORE_SOFTMAX = 0,
+  BSM_SCORE_POINTWISE = 1
+} bsm_score;
+
+/* Mask predicates, AND-ed; flags == 0 is the full mask ([HSTU]
+ * pointwise_splash_attention: MaskType.CAUSAL / FULL, segment ids).
+ *   CAUSAL : key k visible from query q iff k <= q
+ *   LOCAL  : iff q - k < window            (window >= 1)
+ *   SEGMENT: iff q_segment_ids[b][q] == kv_segment_ids[b][k]
+ * Elements past Sq or Skv (a ragged last block) are never visible. */
+#define BSM_MASK_CAUSAL 1u
+#define BSM_MASK_LOCAL 2u
+#define BSM_MASK_SEGMENT 4u
+
+typedef struct bsm_mask_spec {
+  uint32_t flags;
+  int32_t window;  /* used with BSM_MASK_LOCAL only */
+} bsm_mask_spec;
+
+/* Mask-info tables ([HSTU] _next_nonzero; [NOTES] section 21), filled by
+ * bsm_build_mask_info.  All arrays are device memory inside the caller's
+ * buffer.  num_tables is B when SEGMENT is set (one table per batch row),
+ * else 1 (shared by all batch rows and heads).  Row r = t*nq + i.
+ *   block_mask[t][i][j] int8: 0 empty (never loaded), 1 partial (element
+ *                       mask applied), 2 full (no mask)
+ *   data_next[t][i][j]  int32: smallest nonzero j' >= j of row i; if none,
+ *                       the largest nonzero j' < j; 0 for an empty row
+ *   row_ptr[r]          int32, num_tables*nq + 1 entries, CSR offsets
+ *   kv_idx[row_ptr[r]..row_ptr[r+1])  nonzero j of row r, ascending
+ *   kv_cls[...]         their classes (1 or 2)
+ * kv_idx/kv_cls have capacity num_tables*nq*nk. */
+typedef struct bsm_mask_info {
+  uint32_t flags;
+  int32_t window;
+  int32_t num_tables;
+  int32_t Sq, Skv;
+  int32_t block_q, block_kv;
+  int32_t nq, nk; /* ceil(Sq / block_q), ceil(Skv / block_kv) */
+  int8_t* block_mask;
+  int32_t* data_next;
+  int32_t* row_ptr;
+  int32_t* kv_idx;
+  int8_t* kv_cls;
+} bsm_mask_info;
+
+/* Bytes the caller must allocate for bsm_build_mask_info (0 on bad
+ * arguments).  B is the batch size (only used with BSM_MASK_SEGMENT). */
+size_t bsm_mask_info_bytes(const bsm_mask_spec* spec, int32_t B, int32_t Sq,
+                           int32_t Skv, int32_t block_q, int32_t block_kv);
+
+/* Build the mask-info tables on the device ([HSTU] process_mask call in
+ * pointwise_splash_attention; class encoding of _next_nonzero; next-block
+ * table of [NOTES] section 21).  Exact: block classes come from the same
+ * per-element predicate the forward kernel applies.
+ *   q_segment_ids  device int32 [B][Sq], contiguous; required iff SEGMENT
+ *   kv_segment_ids device int32 [B][Skv]; required iff SEGMENT
+ *   block_q, block_kv in {16, 32, 64, 128, 256, 512}
+ *   buffer         device, >= bsm_mask_info_bytes(...) bytes, 256-aligned
+ *   info           host struct, filled with the shape and pointers into
+ *                  `buffer` (valid once the enqueued work has run)
+ * Returns BSM_ERR_INVALID_ARG for non-positive/inconsistent sizes, a
+ * missing or superfluous segment-id array ([HSTU]: both or neither),
+ * window < 1 with LOCAL, or a buffer that is too small or misaligned. */
+bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
+                               const int32_t* q_segment_ids,
+                               const int32_t* kv_segment_ids, int32_t B,
+                               int32_t Sq, int32_t Skv, int32_t block_q,
+                               int32_t block_kv, void* buffer,
+                               size_t buffer_bytes, bsm_mask_info* info,
+                               void* stream);
+
+/* Block-sparse masked attention forward ([NOTES] sections 15, 18, 21;
+ * [HSTU] _pointwise_splash_attention_fwd_kernel_impl).  For each (batch,
+ * head, 128-row query tile) the kernel walks only the KV tiles the mask-info
+ * marks nonzero; full tiles skip the element mask.
+ *   q           device bf16, logical [B][H][Sq][D], head_dim contiguous
+ *   k, v        device bf16, logical [B][H_kv][Skv][D], head_dim contiguous
+ *   *_strides   element strides of the batch, head and sequence dims
+ *               (so [B,H,S,D] and [B,S,H,D] storage both work); every
+ *               stride and pointer must be a multiple of 16 bytes
+ *   H % H_kv == 0: query head h reads K/V head h / (H / H_kv)
+ *   D           64 or 128 (else BSM_ERR_UNSUPPORTED)
+ *   info        from bsm_build_mask_info with the same Sq, Skv, mask and
+ *               (with SEGMENT) the same B; block_q and block_kv must divide
+ *               or be multiples of 128
+ *   q/kv_segment_ids  as for bsm_build_mask_info (required iff SEGMENT)
+ *   scale       logits are scale * q.k ([HSTU] default 1/sqrt(D))
+ *   score       bsm_score
+ *   out         device bf16 [B][H][Sq][D] at o_strides, rounded to nearest
+ *   lse         SOFTMAX: device f32 [B][H][Sq] contiguous, natural-log
+ *               logsumexp of the visible scaled logits (-inf for a row that
+ *               sees no key), or NULL; POINTWISE: must be NULL
+ * Rows that see no key get out = 0.  Returns BSM_ERR_UNSUPPORTED for
+ * Sq > 262144 or Skv > 262144. */
+bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
+                          const int64_t q_strides[3],
+                          const int64_t k_strides[3],
+                          const int64_t v_strides[3],
+                          const int64_t o_strides[3], int32_t B, int32_t H,
+                          int32_t H_kv, int32_t Sq, int32_t Skv, int32_t D,
+                          const bsm_mask_info* info,
+                          const int32_t* q_segment_ids,
+                          const int32_t* kv_segment_ids, float scale,
+                          int32_t score, void* out, float* lse, void* stream);
+
+/* Synchronise `stream` and report whether a kernel of this library gave up
+ * on a bounded wait since the last call (then BSM_ERR_DEVICE_TIMEOUT; the
+ * affected outputs are undefined, the CUDA context stays usable).  If
+ * `detail` is non-NULL it receives 4 ints: code, block, role, phase. */
+bsm_status bsm_device_status(void* stream, int32_t* detail);
+
+/* Failure-detection self test: enqueue one tiny kernel that waits on an
+ * mbarrier nothing ever arrives on, with the given limit in nanoseconds
+ * (1e3..1e10), so that the bounded wait must run out.  A later
+ * bsm_device_status() then returns BSM_ERR_DEVICE_TIMEOUT. */
+bsm_status bsm_selftest_wait_timeout(int64_t timeout_ns, void* stream);
+
+/* Thread-local text of the last error of this thread ("" if none). */
+const char* bsm_last_error(void);
+
+/* ABI version (major*10000 + minor*100 + patch). */
+int32_t bsm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSM_H_ */

@@ -1,0 +1,158 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/bsm.h declares, and rejects bad arguments
+before it touches the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_masked_build_gb300 import build as bsm_build
+from block_sparse_masked_build_gb300 import _lib
+from block_sparse_masked_build_gb300._lib import MaskInfoStruct, MaskSpec, I64x3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsm.h")
+
+INVALID = _lib.BSM_ERR_INVALID_ARG
+UNSUPPORTED = _lib.BSM_ERR_UNSUPPORTED
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bsm_build.build()
+    return _lib.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("bsm_mask_info_bytes", "bsm_build_mask_info", "bsm_splash_fwd",
+              "bsm_device_status", "bsm_last_error", "bsm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert lib.bsm_version() == 100
+
+
+def test_library_is_built_for_sm_103a(lib):
+    # the cubin's target is recorded in the ELF notes; cuobjdump is not
+    # needed: the build command carries exactly one -gencode for sm_103a
+    assert bsm_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+@pytest.mark.parametrize("flags,B,Sq,Skv,bq,bkv", [
+    (1, 4, 2048, 2048, 128, 128), (5, 2, 8192, 8192, 128, 128),
+    (3, 1, 32768, 32768, 128, 128), (1, 1, 256, 256, 64, 64),
+    (4, 3, 700, 300, 64, 32)])
+def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
+    T = B if flags & 4 else 1
+    nq, nk = -(-Sq // bq), -(-Skv // bkv)
+    cells = T * nq * nk
+    want = (_align(cells) + _align(4 * cells) + _align(4 * (T * nq + 1))
+            + _align(4 * cells) + _align(cells))
+    spec = MaskSpec(flags, 4096 if flags & 2 else 0)
+    assert lib.bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv, bq,
+                                   bkv) == want
+
+
+@pytest.mark.parametrize("flags,window,bq,bkv,Sq", [
+    (1, 0, 100, 128, 256), (1, 0, 8, 128, 256), (1, 0, 128, 1024, 256),
+    (2, 0, 128, 128, 256), (8, 0, 128, 128, 256), (1, 0, 128, 128, -1)])
+def test_mask_info_bytes_rejects(lib, flags, window, bq, bkv, Sq):
+    spec = MaskSpec(flags, window)
+    assert lib.bsm_mask_info_bytes(ctypes.byref(spec), 1, Sq, 256, bq,
+                                   bkv) == 0
+
+
+def _build(lib, spec, qs, ks, B, Sq, Skv, bq, bkv, buf, nbytes):
+    info = MaskInfoStruct()
+    return lib.bsm_build_mask_info(
+        None if spec is None else ctypes.byref(spec), qs, ks, B, Sq, Skv, bq,
+        bkv, buf, nbytes, ctypes.byref(info), None)
+
+
+def test_build_mask_info_argument_errors(lib):
+    ok = MaskSpec(1, 0)
+    big = 1 << 30
+    buf = 0x100000  # never dereferenced: every case fails validation first
+    assert _build(lib, None, None, None, 1, 256, 256, 64, 64, buf, big) == INVALID
+    assert _build(lib, MaskSpec(2, 0), None, None, 1, 256, 256, 64, 64, buf,
+                  big) == INVALID
+    assert "window" in _lib.last_error()
+    # segment ids: both or neither (hstu_ops pointwise_splash_attention)
+    assert _build(lib, MaskSpec(4, 0), 0x1000, None, 1, 256, 256, 64, 64, buf,
+                  big) == INVALID
+    assert _build(lib, ok, 0x1000, 0x2000, 1, 256, 256, 64, 64, buf,
+                  big) == INVALID
+    assert "SEGMENT" in _lib.last_error()
+    assert _build(lib, ok, None, None, 1, 256, 256, 64, 64, 0x100010,
+                  big) == INVALID
+    assert "aligned" in _lib.last_error()
+    assert _build(lib, ok, None, None, 1, 256, 256, 64, 64, buf, 16) == INVALID
+    assert "too small" in _lib.last_error()
+    assert _build(lib, ok, None, None, 1, 300000, 256, 64, 64, buf,
+                  big) == UNSUPPORTED
+    assert _build(lib, ok, None, None, 1, 256, 256, 48, 64, buf,
+                  big) == INVALID
+
+
+def _fwd(lib, info, B=1, H=2, Hkv=2, Sq=256, Skv=256, D=128, score=0,
+         lse=None, seg=(None, None), strides=None, q=0x10000):
+    st = strides or (H * Sq * D, Sq * D, D)
+    s3 = I64x3(*st)
+    kv3 = I64x3(Hkv * Skv * D, Skv * D, D)
+    return lib.bsm_splash_fwd(q, 0x20000, 0x30000, s3, kv3, kv3, s3, B, H,
+                              Hkv, Sq, Skv, D, ctypes.byref(info), seg[0],
+                              seg[1], 0.125, score, 0x40000, lse, None)
+
+
+def _info(flags=1, Sq=256, Skv=256, bq=128, bkv=128, tables=1):
+    i = MaskInfoStruct()
+    i.flags, i.window, i.num_tables = flags, 0, tables
+    i.Sq, i.Skv, i.block_q, i.block_kv = Sq, Skv, bq, bkv
+    i.nq, i.nk = -(-Sq // bq), -(-Skv // bkv)
+    i.block_mask = 0x50000
+    return i
+
+
+def test_splash_fwd_argument_errors(lib):
+    info = _info()
+    assert _fwd(lib, info, D=96) == UNSUPPORTED
+    assert "head_dim" in _lib.last_error()
+    assert _fwd(lib, info, H=3, Hkv=2) == INVALID
+    assert _fwd(lib, info, score=1, lse=0x60000) == INVALID
+    assert "logsumexp" in _lib.last_error()
+    assert _fwd(lib, info, score=7) == INVALID
+    assert _fwd(lib, _info(Sq=512)) == INVALID           # info for other Sq
+    assert _fwd(lib, _info(flags=5, tables=1), B=2) == INVALID
+    assert _fwd(lib, _info(flags=5, tables=1)) == INVALID  # no segment ids
+    assert _fwd(lib, info, seg=(0x1000, 0x2000)) == INVALID
+    assert _fwd(lib, info, strides=(2 * 256 * 128, 256 * 128, 100)) == INVALID
+    assert "multiples of 8" in _lib.last_error()
+    assert _fwd(lib, info, q=0x10004) == INVALID
+    assert _fwd(lib, info, Sq=300000, Skv=300000) == UNSUPPORTED
+
+
+def test_splash_fwd_empty_input_is_a_no_op(lib):
+    # B = 0 or Sq = 0: nothing to do, nothing touched
+    assert _fwd(lib, _info(), B=0) == 0
+    assert _fwd(lib, _info(Sq=0, bq=128), Sq=0) == 0
+
+
+def test_selftest_rejects_out_of_range_limits(lib):
+    assert lib.bsm_selftest_wait_timeout(10, None) == INVALID
+    assert lib.bsm_selftest_wait_timeout(10**12, None) == INVALID

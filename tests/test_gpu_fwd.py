@@ -1,0 +1,189 @@
+"""Forward kernel (through the C ABI) vs the fp64 oracle.
+
+Small cases are compared on every output element; they span several
+128-row tiles and KV tiles and end in ragged tails.  The full-size workloads
+run in the launch configuration the benchmark times and are compared on a
+seeded sample of rows (row 0, the last row, block and segment boundaries).
+"""
+
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_sparse_masked_build_gb300 as bsm
+from block_sparse_masked_build_gb300 import workloads as wl
+from gpu_helpers import compare_lse, compare_out, run_gpu, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+C, L, SG = bsm.MASK_CAUSAL, bsm.MASK_LOCAL, bsm.MASK_SEGMENT
+SM, PW = bsm.SCORE_SOFTMAX, bsm.SCORE_POINTWISE
+
+
+def _qkv(B, H, Hkv, Sq, Skv, D, seed, sigma=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, H, Sq, D, generator=g) * sigma).to(torch.bfloat16)
+    k = (torch.randn(B, Hkv, Skv, D, generator=g) * sigma).to(torch.bfloat16)
+    v = (torch.randn(B, Hkv, Skv, D, generator=g) * sigma).to(torch.bfloat16)
+    return q, k, v
+
+
+def _expand_kv(t, H):
+    g = H // t.shape[1]
+    return t.repeat_interleave(g, dim=1)
+
+
+def _check_full(q, k, v, flags, window, sq, skv, scale, score, **kw):
+    out, lse, _ = run_gpu(q, k, v, flags, window, sq, skv, scale, score, **kw)
+    H = q.shape[1]
+    ke, ve = _expand_kv(k, H), _expand_kv(v, H)
+    if score == SM:
+        ref, ref_lse = oracle.softmax_attention(q, ke, ve, flags, window, sq,
+                                                skv, scale)
+        compare_out(out.numpy(), ref, what="softmax")
+        compare_lse(lse.numpy(), ref_lse, what="lse")
+    else:
+        ref = oracle.pointwise_attention(q, ke, ve, flags, window, sq, skv,
+                                         scale)
+        compare_out(out.numpy(), ref, pointwise=True, what="pointwise")
+    return out, lse
+
+
+SMALL = [
+    # name, B, H, Hkv, Sq, Skv, D, flags, window, score, bq, bkv
+    ("cfg1", 1, 2, 2, 256, 256, 64, C, 0, SM, 64, 64),
+    ("causal_ragged_pair", 1, 2, 2, 384, 384, 128, C, 0, SM, 128, 128),
+    ("causal_tail", 2, 1, 1, 300, 300, 128, C, 0, SM, 128, 128),
+    ("full_cross", 1, 2, 2, 200, 333, 128, 0, 0, SM, 128, 128),
+    ("full_cross_d64", 2, 1, 1, 130, 520, 64, 0, 0, SM, 64, 128),
+    ("local_ragged", 1, 2, 2, 1000, 1000, 128, C | L, 300, SM, 128, 128),
+    ("local_bq64", 1, 1, 1, 777, 777, 64, C | L, 129, SM, 64, 64),
+    ("symmetric_band", 1, 1, 1, 600, 600, 128, L, 100, SM, 128, 128),
+    ("pointwise_causal", 1, 2, 2, 384, 384, 128, C, 0, PW, 128, 128),
+    ("pointwise_full_d64", 1, 2, 2, 256, 200, 64, 0, 0, PW, 64, 64),
+    ("gqa", 1, 4, 2, 512, 512, 128, C, 0, SM, 128, 128),
+    ("blocks_256", 1, 2, 2, 768, 768, 128, C, 0, SM, 256, 256),
+    ("blocks_mixed", 1, 2, 2, 640, 640, 128, C, 0, SM, 64, 256),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_cases_elementwise(case):
+    name, B, H, Hkv, Sq, Skv, D, flags, window, score, bq, bkv = case
+    q, k, v = _qkv(B, H, Hkv, Sq, Skv, D, seed=zlib.crc32(name.encode()) % 10000,
+                   sigma=0.5 if score == PW else 1.0)
+    _check_full(q, k, v, flags, window, None, None, 1 / math.sqrt(D), score,
+                block_q=bq, block_kv=bkv)
+
+
+@pytest.mark.parametrize("score", [SM, PW])
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_segments_elementwise(score, causal):
+    B, H, S, D = 2, 2, 640, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=5, sigma=0.5 if score == PW else 1)
+    seg = wl.random_segment_ids(B, S, 20, 300, 9)
+    flags = SG | (C if causal else 0)
+    _check_full(q, k, v, flags, 0, seg, seg, 0.09, score)
+
+
+def test_unsorted_segment_ids_elementwise():
+    B, H, S, D = 1, 2, 512, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=6)
+    rng = np.random.default_rng(3)
+    seg = rng.integers(0, 3, size=(B, S)).astype(np.int32)
+    _check_full(q, k, v, C | SG, 0, seg, seg, 0.1, SM)
+
+
+def test_fully_masked_rows_give_zero_and_neg_inf():
+    B, H, S, D = 1, 1, 256, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=7)
+    qseg = np.zeros((1, S), dtype=np.int32)
+    qseg[0, 30:170] = 9
+    kvseg = np.zeros((1, S), dtype=np.int32)
+    out, lse = _check_full(q, k, v, SG, 0, qseg, kvseg, 0.1, SM)
+    assert torch.all(out[0, 0, 30:170] == 0)
+    assert torch.all(torch.isneginf(lse[0, 0, 30:170]))
+
+
+def test_empty_keys():
+    B, H, Sq, D = 1, 2, 200, 128
+    q, _, _ = _qkv(B, H, H, Sq, 1, D, seed=8)
+    k = torch.empty(B, H, 0, D, dtype=torch.bfloat16)
+    out, lse, _ = run_gpu(q, k, k.clone(), 0, 0, None, None, 0.1, SM)
+    assert torch.all(out == 0)
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_bshd_layout_matches():
+    B, H, S, D = 2, 3, 384, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=9)
+    a, la, _ = run_gpu(q, k, v, C, 0, None, None, 0.1, SM)
+    b, lb, _ = run_gpu(q, k, v, C, 0, None, None, 0.1, SM, layout="bshd")
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+@pytest.mark.parametrize("score", [SM, PW])
+def test_block_size_independence(score):
+    # the result must not depend on the mask-info block sizes
+    B, H, S, D = 1, 2, 512, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=10, sigma=0.5 if score == PW else 1)
+    seg = wl.random_segment_ids(B, S, 30, 200, 11)
+    outs = []
+    for bq, bkv in [(64, 64), (128, 128), (256, 256), (64, 128), (128, 32)]:
+        o, l, _ = run_gpu(q, k, v, C | SG, 0, seg, seg, 0.1, score,
+                          block_q=bq, block_kv=bkv)
+        outs.append((o, l))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0])
+        if score == SM:
+            assert torch.equal(l, outs[0][1])
+
+
+def test_repeated_calls_are_deterministic():
+    B, H, S, D = 2, 4, 1024, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=12)
+    a, la, _ = run_gpu(q, k, v, C, 0, None, None, 0.1, SM)
+    b, lb, _ = run_gpu(q, k, v, C, 0, None, None, 0.1, SM)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+FULL = ["cfg1_causal_s256_d64", "cfg2_causal_s2048_d128",
+        "cfg3_packed_s8192_d128", "cfg3c_causal_s8192_d128",
+        "cfg4_hstu_s4096_d128", "cfg4p_hstu_s4096_d128",
+        "cfg5_local_s32768_d128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled_rows(name):
+    w, q, k, v, seg = workload_inputs(name)
+    out, lse, _ = run_gpu(q, k, v, w.flags, w.window, seg, seg, w.scale,
+                          w.score, block_q=w.block_q, block_kv=w.block_kv)
+    rows = wl.sample_rows(w, 400, seed=123, seg=seg)
+    got = np.stack([out[b, h, r].numpy() for (b, h, r) in rows])
+    if w.score == SM:
+        ref, ref_lse = oracle.softmax_attention(q, k, v, w.flags, w.window,
+                                                seg, seg, w.scale, rows=rows)
+        compare_out(got, ref, what=name)
+        compare_lse(np.array([lse[b, h, r].item() for (b, h, r) in rows]),
+                    ref_lse, what=name)
+        # property at any size: every row is finite and lse is finite
+        assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    else:
+        ref = oracle.pointwise_attention(q, k, v, w.flags, w.window, seg, seg,
+                                         w.scale, rows=rows)
+        compare_out(got, ref, pointwise=True, what=name)
+        assert torch.isfinite(out).all()
+
+
+def test_constant_value_rows_full_size():
+    # invariant at full size (packed segments): constant v rows -> that row
+    w, q, k, _, seg = workload_inputs("cfg3_packed_s8192_d128")
+    c = torch.linspace(-1.5, 2.0, w.D).to(torch.bfloat16)
+    v = c.expand(w.B, w.H, w.S, w.D).contiguous()
+    out, _, _ = run_gpu(q, k, v, w.flags, 0, seg, seg, w.scale, SM)
+    err = (out - c.float()).abs().max().item()
+    assert err <= 2e-2

@@ -1,0 +1,80 @@
+"""Device mask-info builder vs the oracle's brute-force scan: bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import block_sparse_masked_build_gb300 as bsm
+from block_sparse_masked_build_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv):
+    dev = torch.device("cuda")
+    qs = None if seg_q is None else torch.from_numpy(seg_q).to(dev)
+    ks = None if seg_kv is None else torch.from_numpy(seg_kv).to(dev)
+    info = bsm.build_mask_info(flags, B, Sq, Skv, bq, bkv, window, qs, ks,
+                               device=dev)
+    torch.cuda.synchronize()
+    idx, cls = info.kv_lists()
+    return {
+        "block_mask": info.block_mask.cpu().numpy(),
+        "data_next": info.data_next.cpu().numpy(),
+        "row_ptr": info.row_ptr.cpu().numpy(),
+        "kv_idx": idx.cpu().numpy(),
+        "kv_cls": cls.cpu().numpy(),
+    }
+
+
+def _assert_same(got, ref):
+    for key in ("block_mask", "data_next", "row_ptr", "kv_idx", "kv_cls"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workload_mask_info_bit_exact(name):
+    w = wl.WORKLOADS[name]
+    seg = wl.make_segment_ids(w)
+    ref = oracle.mask_info(w.flags, w.window, seg, seg, w.B, w.Sq, w.Skv_,
+                           w.block_q, w.block_kv)
+    got = _gpu_info(w.flags, w.window, seg, seg, w.B, w.Sq, w.Skv_, w.block_q,
+                    w.block_kv)
+    _assert_same(got, ref)
+
+
+CASES = []
+_rng = np.random.default_rng(77)
+for _n in range(40):
+    _flags = int(_rng.choice([0, 1, 2, 3, 4, 5, 6, 7]))
+    _bq = int(_rng.choice([16, 32, 64, 128, 256]))
+    _bkv = int(_rng.choice([16, 32, 64, 128, 256]))
+    _Sq = int(_rng.integers(1, 700))
+    _Skv = _Sq if _flags & 1 else int(_rng.integers(1, 700))
+    CASES.append((_n, _flags, int(_rng.integers(1, 300)), _bq, _bkv, _Sq, _Skv,
+                  int(_rng.integers(1, 4))))
+
+
+@pytest.mark.parametrize("n,flags,window,bq,bkv,Sq,Skv,B", CASES)
+def test_random_tiny_mask_info_bit_exact(n, flags, window, bq, bkv, Sq, Skv, B):
+    rng = np.random.default_rng(1000 + n)
+    seg_q = seg_kv = None
+    if flags & 4:
+        if n % 3 == 0:  # unsorted arbitrary ids
+            seg_q = rng.integers(0, 4, size=(B, Sq)).astype(np.int32)
+            seg_kv = rng.integers(0, 4, size=(B, Skv)).astype(np.int32)
+        else:
+            seg_q = wl.random_segment_ids(B, max(Sq, Skv), 3, 90,
+                                          n)[:, :Sq].copy()
+            seg_kv = wl.random_segment_ids(B, max(Sq, Skv), 3, 90,
+                                           n)[:, :Skv].copy()
+    ref = oracle.mask_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv)
+    got = _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv)
+    _assert_same(got, ref)
+
+
+def test_empty_kv_mask_info():
+    got = _gpu_info(0, 0, None, None, 1, 100, 0, 64, 64)
+    assert got["block_mask"].shape == (1, 2, 0)
+    np.testing.assert_array_equal(got["row_ptr"], [0, 0, 0])
