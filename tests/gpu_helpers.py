@@ -8,10 +8,21 @@ import torch
 import block_sparse_masked_build_gb300 as bsm
 from block_sparse_masked_build_gb300 import workloads as wl
 
-# Tolerances of the forward output (bf16) and the logsumexp (f32).
+# Tolerances of the forward output (bf16) and the logsumexp (f32): max-abs
+# 2e-2 and mean-abs 2e-3 on outputs, 1e-3 relative on logsumexp.
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
 LSE_REL = 1e-3
+# The pointwise path's outputs are ~1e-3 (or ~1e-6 with scale = 1/S), where
+# absolute gates say nothing, so it is also gated relative to the oracle's
+# magnitude: max error <= 2e-2 * max|ref|, and mean error <= 2^-8 * mean|ref|.
+# 2^-8 is two bf16 roundings of at most 2^-9 relative each: P is rounded to
+# bf16 before the P*V product (the precision hstu_ops itself casts p to in
+# its backward, p.astype(do.dtype)) and the output is bf16.  An exact
+# computation with just those two roundings already shows ~2.3e-3 on these
+# shapes.
+PW_MAX_REL = 2e-2
+PW_MEAN_REL = 2.0 ** -8
 
 
 def run_gpu(q, k, v, flags, window, q_seg, kv_seg, scale, score,
@@ -52,10 +63,12 @@ def compare_out(got, ref, pointwise=False, what=""):
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - r)
     if pointwise:
+        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, what
         mx = max(float(np.abs(r).max()), 1e-30)
         mn = max(float(np.abs(r).mean()), 1e-30)
-        assert err.max() / mx <= MAX_ABS, f"{what}: rel max {err.max() / mx}"
-        assert err.mean() / mn <= MEAN_ABS, f"{what}: rel mean {err.mean() / mn}"
+        assert err.max() / mx <= PW_MAX_REL, f"{what}: rel max {err.max() / mx}"
+        assert err.mean() / mn <= PW_MEAN_REL, \
+            f"{what}: rel mean {err.mean() / mn}"
         return err.max() / mx, err.mean() / mn
     assert err.max() <= MAX_ABS, f"{what}: max abs {err.max()}"
     assert err.mean() <= MEAN_ABS, f"{what}: mean abs {err.mean()}"
