@@ -18,6 +18,7 @@ from .api import (  # noqa: F401
     bsm_mask_info_bytes,
     bsm_selftest_wait_timeout,
     bsm_splash_fwd,
+    bsm_splash_fwd_workspace_bytes,
     bsm_version,
     build_mask_info,
     splash_attention,

@@ -11,7 +11,8 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libbsm.so")
+# BSM_LIBRARY may point at another build of the same library.
+LIB_PATH = os.environ.get("BSM_LIBRARY") or os.path.join(HERE, "libbsm.so")
 
 BSM_OK = 0
 BSM_ERR_INVALID_ARG = -1
@@ -48,6 +49,8 @@ class MaskInfoStruct(ctypes.Structure):
         ("row_ptr", ctypes.c_void_p),
         ("kv_idx", ctypes.c_void_p),
         ("kv_cls", ctypes.c_void_p),
+        ("seg_range", ctypes.c_void_p),
+        ("seg_flags", ctypes.c_void_p),
     ]
 
 
@@ -73,11 +76,18 @@ def _declare(lib):
         c.c_void_p, c.c_void_p, c.c_void_p, I64x3, I64x3, I64x3, I64x3,
         c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
         c.POINTER(MaskInfoStruct), c.c_void_p, c.c_void_p, c.c_float,
-        c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p]
+        c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p, c.c_size_t,
+        c.c_void_p]
+    lib.bsm_splash_fwd_workspace_bytes.restype = c.c_size_t
+    lib.bsm_splash_fwd_workspace_bytes.argtypes = []
     lib.bsm_device_status.restype = c.c_int
     lib.bsm_device_status.argtypes = [c.c_void_p, c.POINTER(c.c_int32)]
     lib.bsm_selftest_wait_timeout.restype = c.c_int
     lib.bsm_selftest_wait_timeout.argtypes = [c.c_int64, c.c_void_p]
+    lib.bsm_debug_set_trace.restype = c.c_int
+    lib.bsm_debug_set_trace.argtypes = [c.c_void_p, c.c_size_t]
+    lib.bsm_debug_fwd_grid.restype = c.c_int32
+    lib.bsm_debug_fwd_grid.argtypes = [c.c_int32, c.c_int32, c.c_int32]
     lib.bsm_last_error.restype = c.c_char_p
     lib.bsm_last_error.argtypes = []
     lib.bsm_version.restype = c.c_int32

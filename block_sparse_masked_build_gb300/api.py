@@ -108,6 +108,17 @@ class MaskInfo:
         s = self.struct
         return self._view(s.row_ptr, torch.int32, s.num_tables * s.nq + 1)
 
+    @property
+    def seg_range(self) -> torch.Tensor:
+        """[B, Sq, 2] first/last key with the row's segment id (SEGMENT)."""
+        s = self.struct
+        return self._view(s.seg_range, torch.int32,
+                          s.num_tables * s.Sq * 2).view(s.num_tables, s.Sq, 2)
+
+    @property
+    def seg_flags(self) -> torch.Tensor:
+        return self._view(self.struct.seg_flags, torch.int32, 1)
+
     def kv_lists(self) -> tuple[torch.Tensor, torch.Tensor]:
         """(kv_idx, kv_cls) trimmed to row_ptr[-1] entries (synchronises)."""
         s = self.struct
@@ -137,18 +148,41 @@ def _strides3(t: torch.Tensor):
     return I64x3(t.stride(0), t.stride(1), t.stride(2))
 
 
+def bsm_splash_fwd_workspace_bytes() -> int:
+    return int(_lib.lib().bsm_splash_fwd_workspace_bytes())
+
+
+_workspaces: dict = {}
+
+
+def _default_workspace(device, stream_handle):
+    """One workspace per (device, stream): calls on one stream run in
+    order, so they can share it."""
+    key = (device, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.empty(bsm_splash_fwd_workspace_bytes(), dtype=torch.uint8,
+                         device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def bsm_splash_fwd(q, k, v, mask_info: MaskInfo, q_segment_ids,
                    kv_segment_ids, scale: float, score: int, out,
-                   lse=None, stream=None) -> None:
+                   lse=None, stream=None, workspace=None) -> None:
     """q [B,H,Sq,D], k/v [B,H_kv,Skv,D], out [B,H,Sq,D] (bf16, CUDA)."""
     B, H, Sq, D = q.shape
     H_kv, Skv = k.shape[1], k.shape[2]
+    sh = _stream_handle(stream)
+    if workspace is None:
+        workspace = _default_workspace(q.device, sh)
     _check(_lib.lib().bsm_splash_fwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides3(q), _strides3(k),
         _strides3(v), _strides3(out), B, H, H_kv, Sq, Skv, D,
         ctypes.byref(mask_info.struct), _ptr(q_segment_ids),
         _ptr(kv_segment_ids), float(scale), int(score), out.data_ptr(),
-        _ptr(lse), _stream_handle(stream)))
+        _ptr(lse), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), sh))
 
 
 def bsm_device_status(stream=None) -> tuple[int, list[int]]:
@@ -160,6 +194,42 @@ def bsm_device_status(stream=None) -> tuple[int, list[int]]:
 def bsm_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(_lib.lib().bsm_selftest_wait_timeout(int(timeout_ns),
                                                 _stream_handle(stream)))
+
+
+def bsm_debug_set_trace(buffer) -> None:
+    """Trace the following forward launches into ``buffer`` (a CUDA tensor,
+    16-byte aligned) or switch tracing off with None."""
+    if buffer is None:
+        _check(_lib.lib().bsm_debug_set_trace(None, 0))
+    else:
+        _check(_lib.lib().bsm_debug_set_trace(
+            buffer.data_ptr(), buffer.numel() * buffer.element_size()))
+
+
+def bsm_debug_fwd_grid(B: int, H: int, Sq: int) -> int:
+    return int(_lib.lib().bsm_debug_fwd_grid(B, H, Sq))
+
+
+def decode_trace(buffer, grid: int):
+    """Records of a trace buffer as a list per CTA of
+    (t_ns, role, event, tile, entry, unit), sorted by time."""
+    raw = buffer.cpu().numpy().view("<u8").reshape(-1, 2)
+    per = raw.shape[0] // grid
+    region = (per - 2) // 5
+    out = []
+    for c in range(grid):
+        blk = raw[c * per:(c + 1) * per]
+        counts = blk[0:2].reshape(-1).view("<u4")[:5]
+        recs = []
+        for r, n in enumerate(counts):
+            for i in range(int(n)):
+                row = blk[2 + r * region + i]
+                a = int(row[1] & 0xFFFFFFFF)
+                recs.append((int(row[0]), a >> 28, (a >> 24) & 15,
+                             (a >> 20) & 15, a & 0xFFFFF, int(row[1] >> 32)))
+        recs.sort()
+        out.append(recs)
+    return out
 
 
 # ------------------------------------------------------------ conveniences

@@ -33,10 +33,11 @@ bool is_block_size(int32_t b) {
 }
 
 struct MiLayout {
-  size_t off_bm, off_dn, off_rp, off_idx, off_cls, total;
+  size_t off_bm, off_dn, off_rp, off_idx, off_cls, off_sr, off_sf, total;
 };
 
-MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk) {
+// seg_rows = B * Sq with segment ids, else 0.
+MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows) {
   const size_t cells = static_cast<size_t>(tables * nq * nk);
   const size_t rows = static_cast<size_t>(tables * nq);
   MiLayout L;
@@ -51,6 +52,10 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk) {
   o = align_up(o + cells * 4, 256);
   L.off_cls = o;
   o = align_up(o + cells, 256);
+  L.off_sr = o;
+  o = align_up(o + static_cast<size_t>(seg_rows) * 8, 256);
+  L.off_sf = o;
+  o = align_up(o + 4, 256);
   L.total = o;
   return L;
 }
@@ -153,6 +158,10 @@ uint64_t wait_timeout_ns() {
   return v;
 }
 
+std::mutex g_trace_mu;
+void* g_trace_buf = nullptr;
+size_t g_trace_bytes = 0;
+
 bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
@@ -164,10 +173,12 @@ extern "C" {
 size_t bsm_mask_info_bytes(const bsm_mask_spec* spec, int32_t B, int32_t Sq,
                            int32_t Skv, int32_t block_q, int32_t block_kv) {
   if (check_mi_shape(spec, B, Sq, Skv, block_q, block_kv) != BSM_OK) return 0;
-  const int64_t tables = (spec->flags & BSM_MASK_SEGMENT) ? B : 1;
+  const bool seg = (spec->flags & BSM_MASK_SEGMENT) != 0;
+  const int64_t tables = seg ? B : 1;
   const int64_t nq = (Sq + block_q - 1) / block_q;
   const int64_t nk = (Skv + block_kv - 1) / block_kv;
-  return mi_layout(tables, nq, nk).total;
+  return mi_layout(tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0)
+      .total;
 }
 
 bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
@@ -194,7 +205,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   const int64_t nk = (Skv + block_kv - 1) / block_kv;
   if (tables > 65535)
     return fail(BSM_ERR_UNSUPPORTED, "too many mask tables");
-  const MiLayout L = mi_layout(tables, nq, nk);
+  const MiLayout L =
+      mi_layout(tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0);
   if (buffer == nullptr) return fail(BSM_ERR_INVALID_ARG, "buffer is NULL");
   if ((reinterpret_cast<uintptr_t>(buffer) & 255u) != 0)
     return fail(BSM_ERR_INVALID_ARG, "buffer must be 256-byte aligned");
@@ -221,6 +233,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   mi.row_ptr = reinterpret_cast<int32_t*>(base + L.off_rp);
   mi.kv_idx = reinterpret_cast<int32_t*>(base + L.off_idx);
   mi.kv_cls = reinterpret_cast<int8_t*>(base + L.off_cls);
+  mi.seg_range = reinterpret_cast<int32_t*>(base + L.off_sr);
+  mi.seg_flags = reinterpret_cast<int32_t*>(base + L.off_sf);
 
   bsm::MaskInfoParams p;
   p.flags = mi.flags;
@@ -239,6 +253,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   p.row_ptr = mi.row_ptr;
   p.kv_idx = mi.kv_idx;
   p.kv_cls = mi.kv_cls;
+  p.seg_range = mi.seg_range;
+  p.seg_flags = mi.seg_flags;
   cudaError_t e =
       bsm::launch_mask_info(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mask-info launch");
@@ -255,7 +271,9 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
                           const bsm_mask_info* info,
                           const int32_t* q_segment_ids,
                           const int32_t* kv_segment_ids, float scale,
-                          int32_t score, void* out, float* lse, void* stream) {
+                          int32_t score, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream) {
   g_last_error.clear();
   if (B < 0 || H < 0 || H_kv < 0 || Sq < 0 || Skv < 0)
     return fail(BSM_ERR_INVALID_ARG, "negative size");
@@ -289,12 +307,19 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   if (!seg && (q_segment_ids != nullptr || kv_segment_ids != nullptr))
     return fail(BSM_ERR_INVALID_ARG,
                 "segment ids given without BSM_MASK_SEGMENT");
+  if (seg && (info->seg_range == nullptr || info->seg_flags == nullptr))
+    return fail(BSM_ERR_INVALID_ARG, "mask info lacks segment ranges");
   const int64_t n_super = (Sq + bsm::kUnitRows - 1) / bsm::kUnitRows;
   const int64_t units = static_cast<int64_t>(B) * H * n_super;
   if (units == 0) return BSM_OK;
   if (units > 0x7fffffff) return fail(BSM_ERR_UNSUPPORTED, "too many tiles");
   if (q == nullptr || out == nullptr || (Skv > 0 && (k == nullptr || v == nullptr)))
     return fail(BSM_ERR_INVALID_ARG, "NULL tensor");
+  if (workspace == nullptr || workspace_bytes < bsm::kFwdWorkspaceBytes ||
+      !aligned16(workspace))
+    return fail(BSM_ERR_INVALID_ARG,
+                "workspace must be >= bsm_splash_fwd_workspace_bytes() bytes, "
+                "16-byte aligned");
   if (q_strides == nullptr || k_strides == nullptr || v_strides == nullptr ||
       o_strides == nullptr)
     return fail(BSM_ERR_INVALID_ARG, "NULL strides");
@@ -347,6 +372,8 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.tables = info->num_tables;
   p.q_seg = q_segment_ids;
   p.kv_seg = kv_segment_ids;
+  p.seg_range = info->seg_range;
+  p.seg_flags = info->seg_flags;
   p.score = score;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale = scale;
@@ -356,12 +383,34 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.o_sh = o_strides[1];
   p.o_ss = o_strides[2];
   p.lse = lse;
+  p.unit_counter = static_cast<int32_t*>(workspace);
+  p.lists = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + 256);
+  if (bsm::fwd_grid_size(p, num_sms) > bsm::kMaxCtas)
+    return fail(BSM_ERR_UNSUPPORTED, "more than 256 SMs");
   p.timeout_ns = wait_timeout_ns();
-  cudaError_t e = bsm::launch_splash_fwd(p, tq, tk, tv, num_sms,
-                                         static_cast<cudaStream_t>(stream));
+  p.trace = nullptr;
+  p.trace_cap = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    const int grid = bsm::fwd_grid_size(p, num_sms);
+    if (g_trace_buf != nullptr && grid > 0) {
+      const size_t per = g_trace_bytes / 16 / static_cast<size_t>(grid);
+      if (per >= 7) {
+        p.trace = g_trace_buf;
+        p.trace_cap = static_cast<uint32_t>(per - 2);
+      }
+    }
+  }
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t),
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace reset");
+  e = bsm::launch_splash_fwd(p, tq, tk, tv, num_sms,
+                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "splash_fwd launch");
   return BSM_OK;
 }
+
+size_t bsm_splash_fwd_workspace_bytes(void) { return bsm::kFwdWorkspaceBytes; }
 
 bsm_status bsm_device_status(void* stream, int32_t* detail) {
   g_last_error.clear();
@@ -387,6 +436,24 @@ bsm_status bsm_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
                                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return BSM_OK;
+}
+
+bsm_status bsm_debug_set_trace(void* buffer, size_t bytes) {
+  g_last_error.clear();
+  if (buffer != nullptr && (reinterpret_cast<uintptr_t>(buffer) & 15u) != 0)
+    return fail(BSM_ERR_INVALID_ARG, "trace buffer must be 16-byte aligned");
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_buf = bytes >= 32 ? buffer : nullptr;
+  g_trace_bytes = g_trace_buf != nullptr ? bytes : 0;
+  return BSM_OK;
+}
+
+int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq) {
+  int num_sms = 0;
+  if (check_device(&num_sms) != BSM_OK) return -1;
+  bsm::FwdParams p;
+  p.num_units = B * H * ((Sq + bsm::kUnitRows - 1) / bsm::kUnitRows);
+  return bsm::fwd_grid_size(p, num_sms);
 }
 
 const char* bsm_last_error(void) { return g_last_error.c_str(); }

@@ -1,16 +1,17 @@
 // Block-sparse masked attention forward for sm_103a (GB300).
 //
-// One persistent CTA per SM walks work units of (batch, head, 256 query
-// rows).  A unit is two 128-row query tiles that share one stream of
+// One persistent CTA per SM takes work units of (batch, head, 256 query
+// rows) from a counter in the caller's workspace, heaviest rows first.  A unit is two 128-row query tiles that share one stream of
 // 128-key KV tiles: the union of the nonzero blocks of both tiles, read from
 // the mask-info block classes (hstu_ops `_next_nonzero`: 0 empty, 1
 // partial, 2 full).  Empty KV tiles are never loaded (splash notes section
 // 21); the element mask is evaluated on partial tiles only.
 //
-// Warp roles (320 threads):
-//   warp 0      builds the unit's KV-tile list in shared memory, then issues
-//               TMA loads: Q once per unit, K and V tiles through a ring of
-//               shared-memory slots (128-byte swizzle).
+// Warp roles (352 threads):
+//   warp 10     takes work units from the counter and builds each unit's
+//               KV-tile list, up to two units ahead (three list buffers).
+//   warp 0      issues TMA loads: Q per query tile, K and V tiles through a
+//               ring of shared-memory slots (128-byte swizzle).
 //   warp 1      allocates the 512 TMEM columns and, from one lane, issues the
 //               tcgen05 MMAs: S_t = Q_t K^T (both operands in shared memory)
 //               and O_t += P_t V (P_t read from TMEM, V from shared memory).
@@ -22,6 +23,12 @@
 //               x * sigmoid(x) / Sq with x = scale * q.k, masked -> 0
 //               (hstu_ops fwd kernel).  P goes back to TMEM as bf16 over S.
 // TMEM: S0/P0 cols [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
+//
+// Element mask of a partial tile (hstu_ops `_apply_mask`): each row's visible
+// keys under causal / local masks -- and under segment ids when the kv ids are
+// sorted, via the mask-info's per-row segment ranges -- are one interval, so
+// the mask is a column-range test; unsorted segment ids are compared element
+// by element.  Key indices are the tile's true KV position.
 #include <cstdint>
 
 #include "bsm_internal.h"
@@ -34,33 +41,40 @@ __device__ int g_fwd_error[4];
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3;
+constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3, kRoleList = 4;
 
 template <int D>
 struct Cfg {
   static constexpr int kKBlocks = D / 64;            // 128-byte k-blocks
   static constexpr int kTileBytes = kTileM * D * 2;  // Q, K or V tile
-  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kSlots = (D == 128) ? 5 : 8;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffList = kOffKV + kSlots * kTileBytes;
-  static constexpr int kOffBar = kOffList + 2 * kMaxKvTiles * 4;
+  static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
+};
+static_assert(Cfg<128>::kSmemBytes <= 232448, "shared memory budget");
+
+struct ListMeta {
+  int n;          // entries (KV tiles) of the unit
+  int n_t[2];     // entries used by query tile t
+  int last_t[2];  // index of the last entry used by query tile t (-1: none)
+  int unit;
 };
 
 struct Bars {
-  uint64_t list_full[2], list_free[2];
-  uint64_t q_full, q_empty;
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t list_full[kListBufs], list_free[kListBufs];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[8], kv_empty[8];  // up to 8 ring slots
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
-  int list_count[2];
-  int list_unit[2];
   int abort;
+  uint32_t trace_n[5];
+  ListMeta meta[kListBufs];
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -69,6 +83,42 @@ __device__ __forceinline__ void record_timeout(int role, int phase) {
     g_fwd_error[1] = blockIdx.x;
     g_fwd_error[2] = role;
     g_fwd_error[3] = phase;
+  }
+}
+
+// Optional event trace.  CTA c owns records [c*(cap+2), (c+1)*(cap+2)):
+// records 0-1 hold the event counts of the five roles (uint32 each: load,
+// MMA, score tile 0, score tile 1, list), then come five equal per-role
+// regions, each written by one thread with a plain counter.  A record is
+// {globaltimer ns, role<<28 | event<<24 | tile<<20 | entry, unit}.
+struct TraceRec {
+  uint64_t t;
+  uint32_t a, b;
+};
+enum : uint32_t {
+  kEvListBuilt = 1, kEvQIssued = 2, kEvMmaUnit = 3, kEvMmaLastPv = 4,
+  kEvSFull = 5, kEvPFull = 6, kEvEpiBegin = 7, kEvEpiEnd = 8, kEvRescale = 9,
+  kEvKReady = 10, kEvSIssued = 11, kEvPReady = 12, kEvPVIssued = 13,
+  kEvVReady = 14, kEvTmaIssued = 15
+};
+
+__device__ __forceinline__ void trace(const FwdParams& p, Bars* bars,
+                                      uint32_t role, uint32_t ev, uint32_t tile,
+                                      uint32_t entry, uint32_t unit) {
+  if (p.trace == nullptr) return;
+  const uint32_t slot = role == kRoleScore ? 2 + tile
+                        : role == kRoleMma   ? 1
+                        : role == kRoleList  ? 4
+                                             : 0;
+  const uint32_t per = p.trace_cap / 5;
+  const uint32_t i = bars->trace_n[slot]++;
+  if (i < per) {
+    TraceRec* r = reinterpret_cast<TraceRec*>(p.trace) +
+                  static_cast<size_t>(blockIdx.x) * (p.trace_cap + 2) + 2 +
+                  slot * per + i;
+    r->t = globaltimer_ns();
+    r->a = (role << 28) | (ev << 24) | (tile << 20) | (entry & 0xFFFFFu);
+    r->b = unit;
   }
 }
 
@@ -122,133 +172,227 @@ __device__ __forceinline__ int tile_class(const FwdParams& p, int table,
   return 1;
 }
 
+// Takes the next work unit from the launch's counter and builds its list
+// into buffer ui % 3 (whole warp).  Entries are uint16: kv tile << 4 | class
+// of query tile 0 << 2 | class of tile 1.  When no unit is left the buffer
+// carries unit = -1, which ends every role's loop.
+__device__ __forceinline__ bool build_list(const FwdParams& p, Bars* bars,
+                                           uint16_t* lists, int ui) {
+  const int lane = threadIdx.x % 32;
+  const int buf = ui % kListBufs;
+  if (!warp_wait(&bars->list_free[buf], ((ui / kListBufs) & 1) ^ 1,
+                 &bars->abort, p.timeout_ns)) {
+    if (lane == 0) record_timeout(kRoleList, 0);
+    return false;
+  }
+  int unit = 0;
+  if (lane == 0) unit = atomicAdd(p.unit_counter, 1);
+  unit = __shfl_sync(0xffffffffu, unit, 0);
+  if (unit >= p.num_units) {
+    if (lane == 0) {
+      bars->meta[buf].unit = -1;
+      bars->meta[buf].n = 0;
+      mbar_arrive(&bars->list_full[buf]);
+    }
+    __syncwarp();
+    return true;
+  }
+  const UnitCoord uc = decode_unit(p, unit);
+  const int table = (p.flags & BSM_MASK_SEGMENT) ? uc.b : 0;
+  const int row0 = uc.st * kUnitRows;
+  uint16_t* list = lists + buf * kMaxKvTiles;
+  int n = 0, n0 = 0, n1 = 0, last0 = -1, last1 = -1;
+  for (int base = 0; base < p.n_kvtiles; base += 64) {
+    // two chunks of 32 tiles per pass so that their loads overlap
+    int c[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int jt = base + 32 * h + lane;
+      c[h][0] = c[h][1] = 0;
+      if (jt < p.n_kvtiles) {
+        c[h][0] = tile_class(p, table, row0, jt);
+        c[h][1] = tile_class(p, table, row0 + kTileM, jt);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int jt = base + 32 * h + lane;
+      const int c0 = c[h][0], c1 = c[h][1];
+      const unsigned m = __ballot_sync(0xffffffffu, (c0 | c1) != 0);
+      const int pos = n + __popc(m & ((1u << lane) - 1u));
+      if (c0 | c1)
+        list[pos] = static_cast<uint16_t>((jt << 4) | (c0 << 2) | c1);
+      n0 += __popc(__ballot_sync(0xffffffffu, c0 != 0));
+      n1 += __popc(__ballot_sync(0xffffffffu, c1 != 0));
+      last0 = max(last0, __reduce_max_sync(0xffffffffu, c0 ? pos : -1));
+      last1 = max(last1, __reduce_max_sync(0xffffffffu, c1 ? pos : -1));
+      n += __popc(m);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    ListMeta& mt = bars->meta[buf];
+    mt.n = n;
+    mt.n_t[0] = n0;
+    mt.n_t[1] = n1;
+    mt.last_t[0] = last0;
+    mt.last_t[1] = last1;
+    mt.unit = unit;
+    trace(p, bars, kRoleList, kEvListBuilt, 0, n, unit);
+    mbar_arrive(&bars->list_full[buf]);
+  }
+  __syncwarp();
+  return true;
+}
+
+// List-builder warp: stays up to two units ahead of the consumers.
+__device__ __forceinline__ void list_role(const FwdParams& p, Bars* bars,
+                                         uint16_t* lists) {
+  for (int ui = 0;; ++ui) {
+    if (!build_list(p, bars, lists, ui)) break;
+    if (bars->meta[ui % kListBufs].unit < 0) break;  // sentinel written
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void load_role(const FwdParams& p,
                                           const CUtensorMap* tq,
                                           const CUtensorMap* tk,
                                           const CUtensorMap* tv, uint8_t* smem,
-                                          Bars* bars, uint32_t* lists) {
+                                          Bars* bars, uint16_t* lists) {
   using C = Cfg<D>;
   const int lane = threadIdx.x % 32;
   volatile int* abort_flag = &bars->abort;
   const uint64_t pol_q = l2_policy_evict_first();
   const uint64_t pol_kv = l2_policy_evict_last();
-  uint32_t kv_it = 0, q_it = 0;
-  int ui = 0;
-  for (int unit = blockIdx.x; unit < p.num_units; unit += gridDim.x, ++ui) {
-    const int buf = ui & 1;
-    if (!warp_wait(&bars->list_free[buf], ((ui >> 1) & 1) ^ 1, abort_flag,
-                   p.timeout_ns)) {
+  uint32_t kv_it = 0;
+  uint32_t q_it[2] = {0, 0};
+  bool ok = true;
+  for (int ui = 0; ok; ++ui) {
+    const int buf = ui % kListBufs;
+    ok = warp_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
+                   p.timeout_ns);
+    if (!ok) {
       if (lane == 0) record_timeout(kRoleLoad, 0);
       break;
     }
+    const ListMeta mt = bars->meta[buf];
+    if (mt.unit < 0) break;
+    const int unit = mt.unit;
+    const uint16_t* list = lists + buf * kMaxKvTiles;
     const UnitCoord uc = decode_unit(p, unit);
-    const int table = (p.flags & BSM_MASK_SEGMENT) ? uc.b : 0;
     const int row0 = uc.st * kUnitRows;
-    uint32_t* list = lists + buf * kMaxKvTiles;
-    int n = 0;
-    for (int base = 0; base < p.n_kvtiles; base += 32) {
-      const int jt = base + lane;
-      int c0 = 0, c1 = 0;
-      if (jt < p.n_kvtiles) {
-        c0 = tile_class(p, table, row0, jt);
-        c1 = tile_class(p, table, row0 + kTileM, jt);
-      }
-      const bool nz = (c0 | c1) != 0;
-      const unsigned m = __ballot_sync(0xffffffffu, nz);
-      if (nz) {
-        list[n + __popc(m & ((1u << lane) - 1u))] =
-            (static_cast<uint32_t>(jt) << 4) | (c0 << 2) | c1;
-      }
-      n += __popc(m);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      bars->list_count[buf] = n;
-      bars->list_unit[buf] = unit;
-      mbar_arrive(&bars->list_full[buf]);
-    }
-    if (lane == 0 && n > 0) {
-      bool ok = mbar_wait(&bars->q_empty, (q_it & 1) ^ 1, abort_flag,
-                          p.timeout_ns);
+    // Q, per query tile that has work in this unit
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (!ok || mt.n_t[t] == 0) continue;
+      ok = warp_wait(&bars->q_empty[t], (q_it[t] & 1) ^ 1, abort_flag,
+                     p.timeout_ns);
       if (!ok) {
-        record_timeout(kRoleLoad, 1);
-      } else {
-        const int nt = (row0 + kTileM < p.Sq) ? 2 : 1;
-        mbar_arrive_expect_tx(&bars->q_full, nt * C::kTileBytes);
-        for (int t = 0; t < nt; ++t)
-          for (int kb = 0; kb < C::kKBlocks; ++kb)
-            tma_load_4d(tq, &bars->q_full,
-                        smem + C::kOffQ + t * C::kTileBytes + kb * kTileM * 128,
-                        kb * 64, row0 + t * kTileM, uc.h, uc.b, pol_q);
-        ++q_it;
-        const int hkv = uc.h / (p.H / p.Hkv);
-        for (int e = 0; e < n && ok; ++e) {
-          const int jt = static_cast<int>(list[e] >> 4);
-          for (int which = 0; which < 2 && ok; ++which) {
-            const int slot = kv_it % C::kSlots;
-            const uint32_t ph = (kv_it / C::kSlots) & 1;
-            ok = mbar_wait(&bars->kv_empty[slot], ph ^ 1, abort_flag,
-                           p.timeout_ns);
-            if (!ok) {
-              record_timeout(kRoleLoad, 2);
-              break;
-            }
-            mbar_arrive_expect_tx(&bars->kv_full[slot], C::kTileBytes);
-            uint8_t* dst = smem + C::kOffKV + slot * C::kTileBytes;
-            for (int kb = 0; kb < C::kKBlocks; ++kb)
-              tma_load_4d(which == 0 ? tk : tv, &bars->kv_full[slot],
-                          dst + kb * kTileN * 128, kb * 64, jt * kTileN, hkv,
-                          uc.b, pol_kv);
-            ++kv_it;
-          }
+        if (lane == 0) record_timeout(kRoleLoad, 1);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
+        for (int kb = 0; kb < C::kKBlocks; ++kb)
+          tma_load_4d(tq, &bars->q_full[t],
+                      smem + C::kOffQ + t * C::kTileBytes + kb * kTileM * 128,
+                      kb * 64, row0 + t * kTileM, uc.h, uc.b, pol_q);
+        trace(p, bars, kRoleLoad, kEvQIssued, t, 0, unit);
+      }
+      ++q_it[t];
+    }
+    const int hkv = uc.h / (p.H / p.Hkv);
+    for (int e = 0; ok && e < mt.n; ++e) {
+      const int jt = static_cast<int>(list[e] >> 4);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        if (!ok) break;
+        const int slot = kv_it % C::kSlots;
+        const uint32_t ph = (kv_it / C::kSlots) & 1;
+        ok = warp_wait(&bars->kv_empty[slot], ph ^ 1, abort_flag,
+                       p.timeout_ns);
+        if (!ok) {
+          if (lane == 0) record_timeout(kRoleLoad, 2);
+          break;
         }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->kv_full[slot], C::kTileBytes);
+          uint8_t* dst = smem + C::kOffKV + slot * C::kTileBytes;
+          for (int kb = 0; kb < C::kKBlocks; ++kb)
+            tma_load_4d(which == 0 ? tk : tv, &bars->kv_full[slot],
+                        dst + kb * kTileN * 128, kb * 64, jt * kTileN, hkv,
+                        uc.b, pol_kv);
+          trace(p, bars, kRoleLoad, kEvTmaIssued, which, e, unit);
+        }
+        ++kv_it;
       }
     }
     __syncwarp();
-    if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+    if (lane == 0) mbar_arrive(&bars->list_free[buf]);
   }
 }
 
 template <int D>
 __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
-                                         Bars* bars, const uint32_t* lists,
+                                         Bars* bars, const uint16_t* lists,
                                          uint32_t tmem) {
   using C = Cfg<D>;
   volatile int* abort_flag = &bars->abort;
-  const uint32_t q_base = smem_u32(smem + C::kOffQ);
-  const uint32_t kv_base = smem_u32(smem + C::kOffKV);
   constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, true);
-  uint32_t kv_it = 0, q_it = 0;
-  uint32_t s_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
-  int ui = 0;
+  // Descriptors of the tile bases; a K-step only adds to the start-address
+  // field (16-byte units), which never carries into the upper fields.
+  const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+  const uint64_t dkv0 = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
+  const uint64_t dv0 =
+      sdesc_sw128(smem_u32(smem + C::kOffKV), kTileN * 128, 1024);
+  constexpr uint32_t kTileUnits = C::kTileBytes >> 4;
+  uint32_t kv_it = 0;
+  uint32_t q_it[2] = {0, 0};
+  uint32_t s_cnt[2] = {0, 0};
   bool ok = true;
-  for (int unit = blockIdx.x; unit < p.num_units && ok;
-       unit += gridDim.x, ++ui) {
-    const int buf = ui & 1;
-    ok = mbar_wait(&bars->list_full[buf], (ui >> 1) & 1, abort_flag,
+
+  // S_t = Q_t K^T for the K tile in `kslot`.
+  auto issue_s = [&](int t, int kslot) {
+    const uint64_t a = dq0 + t * kTileUnits;
+    const uint64_t b = dkv0 + kslot * kTileUnits;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+      mma_ss(tmem + t * 128, a + off, b + off, idesc_s, k > 0 ? 1u : 0u);
+    }
+    mma_commit(&bars->s_full[t]);
+    ++s_cnt[t];
+  };
+
+  for (int ui = 0; ok; ++ui) {
+    const int buf = ui % kListBufs;
+    ok = mbar_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
                    p.timeout_ns);
     if (!ok) {
       record_timeout(kRoleMma, 0);
       break;
     }
-    const int n = bars->list_count[buf];
-    const uint32_t* list = lists + buf * kMaxKvTiles;
-    if (n > 0) {
-      ok = mbar_wait(&bars->q_full, q_it & 1, abort_flag, p.timeout_ns);
-      if (!ok) {
-        record_timeout(kRoleMma, 1);
-        break;
-      }
-      tc_fence_after();
-      bool first_pv[2] = {true, true};
-      for (int e = 0; e < n && ok; ++e) {
-        const uint32_t ent = list[e];
-        const int cls[2] = {static_cast<int>((ent >> 2) & 3u),
-                            static_cast<int>(ent & 3u)};
-        // ---- S_t = Q_t K^T
-        const int kslot = kv_it % C::kSlots;
+    const ListMeta mt = bars->meta[buf];
+    if (mt.unit < 0) break;
+    const int unit = mt.unit;
+    const uint16_t* list = lists + buf * kMaxKvTiles;
+    trace(p, bars, kRoleMma, kEvMmaUnit, 0, mt.n, unit);
+    bool q_ready[2] = {false, false};
+    bool first_pv[2] = {true, true};
+    bool s_ahead[2] = {false, false};  // S_t of the current entry already issued
+    int kslot_next = -1;               // K slot of entry e+1 if already waited
+    uint32_t nxt = mt.n > 0 ? list[0] : 0u;  // list entries are read one ahead
+    for (int e = 0; e < mt.n && ok; ++e) {
+      const uint32_t ent = nxt;
+      const bool use[2] = {((ent >> 2) & 3u) != 0, (ent & 3u) != 0};
+      nxt = (e + 1 < mt.n) ? list[e + 1] : 0u;
+      const bool use_next[2] = {((nxt >> 2) & 3u) != 0, (nxt & 3u) != 0};
+      // ---- K of this entry, and S_t for the tiles not issued ahead
+      int kslot = kslot_next;
+      if (kslot < 0) {
+        kslot = kv_it % C::kSlots;
         ok = mbar_wait(&bars->kv_full[kslot], (kv_it / C::kSlots) & 1,
                        abort_flag, p.timeout_ns);
         if (!ok) {
@@ -256,72 +400,101 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
           break;
         }
         ++kv_it;
-        tc_fence_after();
+        trace(p, bars, kRoleMma, kEvKReady, 0, e, unit);
+      }
+      kslot_next = -1;
+      tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!cls[t] || !ok) continue;
-          if (pv_cnt[t] > 0) {  // P_t (aliasing S_t) consumed by the last PV
-            ok = mbar_wait(&bars->pv_done[t], (pv_cnt[t] - 1) & 1, abort_flag,
-                           p.timeout_ns);
-            if (!ok) {
-              record_timeout(kRoleMma, 3);
-              break;
-            }
-            tc_fence_after();
-          }
-          const uint32_t a0 = q_base + t * C::kTileBytes;
-          const uint32_t b0 = kv_base + kslot * C::kTileBytes;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * (kTileM * 128) + (k & 3) * 32;
-            mma_ss(tmem + t * 128, sdesc_sw128(a0 + off, 16, 1024),
-                   sdesc_sw128(b0 + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->s_full[t]);
-          ++s_cnt[t];
-        }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[kslot]);
-        // ---- O_t += P_t V
-        const int vslot = kv_it % C::kSlots;
-        ok = mbar_wait(&bars->kv_full[vslot], (kv_it / C::kSlots) & 1,
-                       abort_flag, p.timeout_ns);
-        if (!ok) {
-          record_timeout(kRoleMma, 4);
-          break;
-        }
-        ++kv_it;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!cls[t] || !ok) continue;
-          ok = mbar_wait(&bars->p_full[t], (s_cnt[t] - 1) & 1, abort_flag,
+      for (int t = 0; t < 2; ++t) {
+        if (!use[t] || s_ahead[t] || !ok) continue;
+        if (!q_ready[t]) {
+          ok = mbar_wait(&bars->q_full[t], q_it[t] & 1, abort_flag,
                          p.timeout_ns);
-          if (ok && first_pv[t])
-            ok = mbar_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
-                           p.timeout_ns);
+          q_ready[t] = true;
           if (!ok) {
-            record_timeout(kRoleMma, 5);
+            record_timeout(kRoleMma, 1);
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = kv_base + vslot * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                   sdesc_sw128(b0 + kk * 16 * 128, kTileN * 128, 1024),
-                   idesc_o, (first_pv[t] && kk == 0) ? 0u : 1u);
-          }
-          first_pv[t] = false;
-          mma_commit(&bars->pv_done[t]);
-          ++pv_cnt[t];
         }
-        if (!ok) break;
-        mma_commit(&bars->kv_empty[vslot]);
+        issue_s(t, kslot);
+        trace(p, bars, kRoleMma, kEvSIssued, t, e, unit);
       }
       if (!ok) break;
-      mma_commit(&bars->q_empty);
-      ++q_it;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (use[t] && e == mt.last_t[t]) {  // Q_t of this unit not needed
+          mma_commit(&bars->q_empty[t]);
+          ++q_it[t];
+        }
+      }
+      // every S MMA that reads this K tile has been issued
+      mma_commit(&bars->kv_empty[kslot]);
+      // ---- V of this entry; O_t += P_t V, then S_t of the next entry
+      const int vslot = kv_it % C::kSlots;
+      ok = mbar_wait(&bars->kv_full[vslot], (kv_it / C::kSlots) & 1,
+                     abort_flag, p.timeout_ns);
+      if (!ok) {
+        record_timeout(kRoleMma, 4);
+        break;
+      }
+      ++kv_it;
+      trace(p, bars, kRoleMma, kEvVReady, 0, e, unit);
+      s_ahead[0] = s_ahead[1] = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!use[t] || !ok) continue;
+        ok = mbar_wait(&bars->p_full[t], (s_cnt[t] - 1) & 1, abort_flag,
+                       p.timeout_ns);
+        if (ok && first_pv[t])
+          ok = mbar_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
+                         p.timeout_ns);
+        if (!ok) {
+          record_timeout(kRoleMma, 5);
+          break;
+        }
+        trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
+        tc_fence_after();
+        const uint64_t b = dv0 + vslot * kTileUnits;
+        const uint32_t o_acc = tmem + 256 + t * 128;
+        const uint32_t p_tm = tmem + t * 128;
+        if (first_pv[t]) {
+          mma_ts(o_acc, p_tm, b, idesc_o, 0u);
+        } else {
+          mma_ts(o_acc, p_tm, b, idesc_o, 1u);
+        }
+#pragma unroll
+        for (int kk = 1; kk < kTileN / 16; ++kk)
+          mma_ts(o_acc, p_tm + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
+        first_pv[t] = false;
+        mma_commit(&bars->pv_done[t]);
+        trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
+        // S_t of the next entry goes right behind this tile's P.V.  It
+        // overwrites the TMEM columns the P.V just read: tcgen05.mma
+        // instructions of one thread run in the order they were issued.
+        if (use_next[t]) {
+          if (kslot_next < 0) {
+            kslot_next = kv_it % C::kSlots;
+            ok = mbar_wait(&bars->kv_full[kslot_next],
+                           (kv_it / C::kSlots) & 1, abort_flag, p.timeout_ns);
+            if (!ok) {
+              record_timeout(kRoleMma, 2);
+              break;
+            }
+            ++kv_it;
+            trace(p, bars, kRoleMma, kEvKReady, 0, e + 1, unit);
+            tc_fence_after();
+          }
+          issue_s(t, kslot_next);
+          s_ahead[t] = true;
+          trace(p, bars, kRoleMma, kEvSIssued, t, e + 1, unit);
+        }
+      }
+      if (!ok) break;
+      mma_commit(&bars->kv_empty[vslot]);
     }
+    if (!ok) break;
+    trace(p, bars, kRoleMma, kEvMmaLastPv, 0, mt.n, unit);
     mbar_arrive(&bars->list_free[buf]);
   }
   // Drain: every MMA issued above has completed once this arrives.
@@ -330,124 +503,142 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
     record_timeout(kRoleMma, 6);
 }
 
-// Element mask of a partial tile for one query row (hstu_ops `_apply_mask`:
-// the computed causal/local predicate AND q_seg == kv_seg, with key indices
-// taken from the true KV position of the tile, not its list position).
-struct RowMask {
-  int lo_c, hi_c;  // visible columns c of the tile satisfy lo_c <= c <= hi_c
-  int segq;
-  const int32_t* segk;  // kv segment ids of the tile's first key, or null
-};
-
-__device__ __forceinline__ RowMask row_mask(const FwdParams& p, int qrow, int b,
-                                            int jt) {
-  const int kbase = jt * kTileN;
-  int hi_k = p.Skv - 1;
-  int lo_k = 0;
-  if (p.flags & BSM_MASK_CAUSAL) hi_k = min(hi_k, qrow);
-  if (p.flags & BSM_MASK_LOCAL) lo_k = max(lo_k, qrow - p.window + 1);
-  RowMask m;
-  m.lo_c = lo_k - kbase;
-  m.hi_c = hi_k - kbase;
-  m.segq = 0;
-  m.segk = nullptr;
-  if (p.flags & BSM_MASK_SEGMENT) {
-    m.segk = p.kv_seg + static_cast<int64_t>(b) * p.Skv + kbase;
+// "Same segment" bits of the 128 keys of a tile for one row (unsorted
+// segment ids), one 32-bit word per 32 keys.  Computed before S is loaded
+// from TMEM, so the loads never compete with S for registers.
+__device__ __forceinline__ void segment_bits(uint32_t keep[4],
+                                             const int32_t* segk, int nvalid,
+                                             int segq) {
+  const bool vec =
+      nvalid == kTileN && (reinterpret_cast<uintptr_t>(segk) & 15u) == 0;
+#pragma unroll 1
+  for (int w = 0; w < kTileN / 32; ++w) {
+    uint32_t bits = 0;
+    if (vec) {
+      const int4* s4 = reinterpret_cast<const int4*>(segk + 32 * w);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const int4 v = __ldg(s4 + c4);
+        bits |= (v.x == segq ? 1u : 0u) << (4 * c4);
+        bits |= (v.y == segq ? 1u : 0u) << (4 * c4 + 1);
+        bits |= (v.z == segq ? 1u : 0u) << (4 * c4 + 2);
+        bits |= (v.w == segq ? 1u : 0u) << (4 * c4 + 3);
+      }
+    } else {
+#pragma unroll 8
+      for (int c = 0; c < 32; ++c) {
+        const int k = 32 * w + c;
+        if (k < nvalid && __ldg(segk + k) == segq) bits |= 1u << c;
+      }
+    }
+    keep[0] = w == 0 ? bits : keep[0];
+    keep[1] = w == 1 ? bits : keep[1];
+    keep[2] = w == 2 ? bits : keep[2];
+    keep[3] = w == 3 ? bits : keep[3];
   }
-  return m;
 }
 
-// Visibility of the 4 columns c..c+3 as bits (segment ids read 4 at a time;
-// the last KV tile is only read below hi_c, which stays inside the keys).
-__device__ __forceinline__ uint32_t vis4(const RowMask& m, int c) {
-  uint32_t bits = 0;
+// Masks S of a partial tile in place: columns outside [lo_c, hi_c] or with a
+// cleared keep bit become -inf.
+__device__ __forceinline__ void mask_tile(float* s, int lo_c, int hi_c,
+                                          const uint32_t keep[4]) {
+  const float NEG_INF = __int_as_float(0xff800000);
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
-    bits |= ((c + u >= m.lo_c) && (c + u <= m.hi_c)) ? (1u << u) : 0u;
-  if (m.segk != nullptr && bits) {
-    int4 s;
-    if (c + 3 <= m.hi_c &&
-        (reinterpret_cast<uintptr_t>(m.segk + c) & 15u) == 0) {
-      s = __ldg(reinterpret_cast<const int4*>(m.segk + c));
-    } else {
-      s.x = m.segk[c];
-      s.y = (c + 1 <= m.hi_c) ? m.segk[c + 1] : 0;
-      s.z = (c + 2 <= m.hi_c) ? m.segk[c + 2] : 0;
-      s.w = (c + 3 <= m.hi_c) ? m.segk[c + 3] : 0;
-    }
-    bits &= (s.x == m.segq ? 1u : 0u) | (s.y == m.segq ? 2u : 0u) |
-            (s.z == m.segq ? 4u : 0u) | (s.w == m.segq ? 8u : 0u);
+  for (int c = 0; c < kTileN; ++c) {
+    const bool vis = (c >= lo_c) && (c <= hi_c) &&
+                     ((keep[c / 32] >> (c % 32)) & 1u);
+    s[c] = vis ? s[c] : NEG_INF;
   }
-  return bits;
 }
 
 template <int D, int SCORE>
 __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
-                                           const uint32_t* lists,
+                                           const uint16_t* lists,
                                            uint32_t tmem) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = (warp - 2) / 4;  // query tile of this warpgroup
   const int quarter = warp % 4;  // TMEM lane quarter this warp may access
   const int r = quarter * 32 + lane;
+  const bool tracer = (r == 0);
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t s_addr = tmem + lane_off + t * 128;
   const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
   volatile int* abort_flag = &bars->abort;
   const float NEG_INF = __int_as_float(0xff800000);
+  const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
+  const bool seg_elem = seg && (*p.seg_flags & 1) != 0;
   uint32_t s_cnt = 0, pv_cnt = 0;
-  int ui = 0;
-  for (int unit = blockIdx.x; unit < p.num_units; unit += gridDim.x, ++ui) {
-    const int buf = ui & 1;
-    if (!warp_wait(&bars->list_full[buf], (ui >> 1) & 1, abort_flag,
+  for (int ui = 0;; ++ui) {
+    const int buf = ui % kListBufs;
+    if (!warp_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
                    p.timeout_ns)) {
       record_timeout(kRoleScore, 0);
       break;
     }
-    const int n = bars->list_count[buf];
-    const UnitCoord uc = decode_unit(p, bars->list_unit[buf]);
-    const uint32_t* list = lists + buf * kMaxKvTiles;
+    const ListMeta mt = bars->meta[buf];
+    if (mt.unit < 0) break;
+    const UnitCoord uc = decode_unit(p, mt.unit);
+    const uint16_t* list = lists + buf * kMaxKvTiles;
     const int qrow = uc.st * kUnitRows + t * kTileM + r;
+    const bool row_ok = qrow < p.Sq;
+    // visible keys of this row form [rlo, rhi] (plus the element compare of
+    // unsorted segment ids)
+    int rlo = 0, rhi = p.Skv - 1;
+    if (p.flags & BSM_MASK_CAUSAL) rhi = min(rhi, qrow);
+    if (p.flags & BSM_MASK_LOCAL) rlo = max(rlo, qrow - p.window + 1);
     int segq = 0;
-    if ((p.flags & BSM_MASK_SEGMENT) && qrow < p.Sq)
-      segq = p.q_seg[static_cast<int64_t>(uc.b) * p.Sq + qrow];
+    if (seg && row_ok) {
+      const int64_t qi = static_cast<int64_t>(uc.b) * p.Sq + qrow;
+      if (seg_elem) {
+        segq = p.q_seg[qi];
+      } else {
+        const int2 sr = reinterpret_cast<const int2*>(p.seg_range)[qi];
+        rlo = max(rlo, sr.x);
+        rhi = min(rhi, sr.y);
+      }
+    }
+    const int32_t* segk_b =
+        seg_elem ? p.kv_seg + static_cast<int64_t>(uc.b) * p.Skv : nullptr;
     float m_used = NEG_INF, l_sum = 0.f;
     uint32_t unit_pv = 0;
     bool ok = true;
-    for (int e = 0; e < n; ++e) {
+    for (int e = 0; e < mt.n; ++e) {
       const uint32_t ent = list[e];
       const int cls = t == 0 ? static_cast<int>((ent >> 2) & 3u)
                              : static_cast<int>(ent & 3u);
       if (!cls) continue;
       const int jt = static_cast<int>(ent >> 4);
+      const int kbase = jt * kTileN;
+      uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (cls == 1 && seg_elem)
+        segment_bits(keep, segk_b + kbase, min(kTileN, p.Skv - kbase), segq);
       ok = warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, p.timeout_ns);
       if (!ok) {
         record_timeout(kRoleScore, 1);
         break;
       }
       ++s_cnt;
+      if (tracer) trace(p, bars, kRoleScore, kEvSFull, t, e, mt.unit);
       tc_fence_after();
       uint32_t sraw[kTileN];
 #pragma unroll
-      for (int q = 0; q < kTileN / 32; ++q) tmem_ld32(s_addr + q * 32, sraw + q * 32);
+      for (int q = 0; q < kTileN / 32; ++q)
+        tmem_ld32(s_addr + q * 32, sraw + q * 32);
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sraw);
+      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep);
 
-      uint32_t pk[kTileN / 2];
+      uint32_t pk[16];
       if (SCORE == BSM_SCORE_SOFTMAX) {
-        if (cls == 1) {
-          RowMask mk = row_mask(p, qrow, uc.b, jt);
-          mk.segq = segq;
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-          for (int c = 0; c < kTileN; c += 4) {
-            const uint32_t bits = vis4(mk, c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (!(bits & (1u << u))) s[c + u] = NEG_INF;
-          }
+        for (int c = 4; c < kTileN; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
         }
-        float mx = s[0];
-#pragma unroll
-        for (int c = 1; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_blk = mx * p.scale_log2;
         bool rescale = false;
         float alpha = 1.f;
@@ -460,17 +651,25 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
           m_used = m_blk;
         }
         const float neg_m = (m_used == NEG_INF) ? 0.f : -m_used;
-        float lsum = 0.f;
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kTileN; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
-          lsum += p0 + p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int q = 0; q < kTileN / 32; ++q) {  // 32 columns at a time
+#pragma unroll
+          for (int c = 32 * q; c < 32 * q + 32; c += 4) {
+            const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
+            const float p2 = ex2_approx(fmaf(s[c + 2], p.scale_log2, neg_m));
+            const float p3 = ex2_approx(fmaf(s[c + 3], p.scale_log2, neg_m));
+            ls0 += p0;
+            ls1 += p1;
+            ls2 += p2;
+            ls3 += p3;
+            pk[(c & 31) / 2] = pack_bf16x2(p0, p1);
+            pk[(c & 31) / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(s_addr + q * 16, pk);
         }
-        l_sum += lsum;
-#pragma unroll
-        for (int q = 0; q < kTileN / 32; ++q) tmem_st16(s_addr + q * 16, pk + q * 16);
+        l_sum += (ls0 + ls1) + (ls2 + ls3);
         // Rescale O_t (needs the previous PV of this tile to have landed).
         if (__any_sync(0xffffffffu, rescale) && unit_pv > 0) {
           ok = warp_wait(&bars->pv_done[t], (pv_cnt - 1) & 1, abort_flag,
@@ -479,6 +678,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
             record_timeout(kRoleScore, 2);
             break;
           }
+          if (tracer) trace(p, bars, kRoleScore, kEvRescale, t, e, mt.unit);
           tc_fence_after();
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
@@ -492,38 +692,35 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
           }
         }
       } else {
-        // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked -> 0
-        RowMask mk;
-        if (cls == 1) {
-          mk = row_mask(p, qrow, uc.b, jt);
-          mk.segq = segq;
-        }
+        // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked (-inf) -> 0
 #pragma unroll
-        for (int c = 0; c < kTileN; c += 4) {
-          const uint32_t bits = (cls == 1) ? vis4(mk, c) : 0xfu;
-          float pv[4];
+        for (int q = 0; q < kTileN / 32; ++q) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float x = s[c + u] * p.scale;
-            const float sg = rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x));
-            pv[u] = (bits & (1u << u)) ? x * sg * p.inv_sq : 0.f;
+          for (int c = 32 * q; c < 32 * q + 32; c += 2) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float x = s[c + u] * p.scale;
+              const float sg =
+                  rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x));
+              pv[u] = (s[c + u] != NEG_INF) ? x * sg * p.inv_sq : 0.f;
+            }
+            pk[(c & 31) / 2] = pack_bf16x2(pv[0], pv[1]);
           }
-          pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          tmem_st16(s_addr + q * 16, pk);
         }
-#pragma unroll
-        for (int q = 0; q < kTileN / 32; ++q) tmem_st16(s_addr + q * 16, pk + q * 16);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
+      if (tracer) trace(p, bars, kRoleScore, kEvPFull, t, e, mt.unit);
       ++pv_cnt;
       ++unit_pv;
     }
     if (!ok) break;
 
     // ---- epilogue: out = O / l (softmax) or O (pointwise), bf16
-    const bool row_ok = qrow < p.Sq;
+    if (tracer) trace(p, bars, kRoleScore, kEvEpiBegin, t, 0, mt.unit);
     uint16_t* orow = p.out + static_cast<int64_t>(uc.b) * p.o_sb +
                      static_cast<int64_t>(uc.h) * p.o_sh +
                      static_cast<int64_t>(qrow) * p.o_ss;
@@ -566,6 +763,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
     tc_fence_before();
     mbar_arrive(&bars->o_free[t]);
     mbar_arrive(&bars->list_free[buf]);
+    if (tracer) trace(p, bars, kRoleScore, kEvEpiEnd, t, 0, mt.unit);
   }
 }
 
@@ -580,26 +778,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
-  uint32_t* lists = reinterpret_cast<uint32_t*>(smem + C::kOffList);
+  uint16_t* lists = p.lists + static_cast<size_t>(blockIdx.x) * kListBufs *
+                                  kMaxKvTiles;
   const int warp = threadIdx.x / 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kListBufs; ++i) {
       mbar_init(&bars->list_full[i], 1);
-      mbar_init(&bars->list_free[i], 1 + 2 * kTileM);
+      mbar_init(&bars->list_free[i], 2 + 2 * kTileM);  // load, MMA, score
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], kTileM);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->o_free[i], kTileM);
     }
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
+    for (int i = 0; i < 5; ++i) bars->trace_n[i] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -616,6 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     load_role<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, lists);
+  } else if (warp == 10) {
+    list_role(p, bars, lists);
   } else if (warp == 1) {
     if ((threadIdx.x % 32) == 0) mma_role<D>(p, smem, bars, lists, tmem);
     __syncwarp();
@@ -627,18 +831,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (p.trace != nullptr && threadIdx.x == 0) {
+    uint32_t* hdr = reinterpret_cast<uint32_t*>(
+        reinterpret_cast<TraceRec*>(p.trace) +
+        static_cast<size_t>(blockIdx.x) * (p.trace_cap + 2));
+    const uint32_t per = p.trace_cap / 5;
+    for (int i = 0; i < 8; ++i) hdr[i] = i < 5 ? min(bars->trace_n[i], per) : 0;
+  }
 }
 
 template <int D, int SCORE>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv,
-                       int num_sms, cudaStream_t stream) {
+                       int grid, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = splash_fwd_kernel<D, SCORE>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -661,16 +871,21 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns) {
 
 }  // namespace
 
+int fwd_grid_size(const FwdParams& p, int num_sms) {
+  return p.num_units < num_sms ? p.num_units : num_sms;
+}
+
 cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               int num_sms, cudaStream_t stream) {
+  const int grid = fwd_grid_size(p, num_sms);
   const bool pw = p.score == BSM_SCORE_POINTWISE;
   if (p.D == 128)
-    return pw ? launch_one<128, BSM_SCORE_POINTWISE>(p, tq, tk, tv, num_sms, stream)
-              : launch_one<128, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, num_sms, stream);
+    return pw ? launch_one<128, BSM_SCORE_POINTWISE>(p, tq, tk, tv, grid, stream)
+              : launch_one<128, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, grid, stream);
   if (p.D == 64)
-    return pw ? launch_one<64, BSM_SCORE_POINTWISE>(p, tq, tk, tv, num_sms, stream)
-              : launch_one<64, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, num_sms, stream);
+    return pw ? launch_one<64, BSM_SCORE_POINTWISE>(p, tq, tk, tv, grid, stream)
+              : launch_one<64, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, grid, stream);
   return cudaErrorInvalidValue;
 }
 

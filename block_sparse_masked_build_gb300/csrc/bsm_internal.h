@@ -18,6 +18,13 @@ constexpr int kTileN = 128;
 constexpr int kUnitRows = 2 * kTileM;
 constexpr int kMaxSeq = 262144;
 constexpr int kMaxKvTiles = kMaxSeq / kTileN;  // list capacity per unit
+// Forward workspace: 256 bytes of counters, then per CTA three unit lists of
+// kMaxKvTiles uint16 entries (up to kMaxCtas CTAs).
+constexpr int kMaxCtas = 256;
+constexpr int kListBufs = 3;
+constexpr size_t kListBytes = static_cast<size_t>(kMaxKvTiles) * 2;
+constexpr size_t kFwdWorkspaceBytes =
+    256 + static_cast<size_t>(kMaxCtas) * kListBufs * kListBytes;
 
 struct MaskInfoParams {
   uint32_t flags;
@@ -30,6 +37,8 @@ struct MaskInfoParams {
   int32_t* row_ptr;
   int32_t* kv_idx;
   int8_t* kv_cls;
+  int32_t* seg_range;  // [tables][Sq][2] (SEGMENT only)
+  int32_t* seg_flags;  // [1]: bit 0 = some kv id row is not sorted
 };
 
 struct FwdParams {
@@ -42,8 +51,10 @@ struct FwdParams {
   int32_t window;
   const int8_t* block_mask;  // [tables][mi_nq][mi_nk]
   int32_t mi_nq, mi_nk, bq, bkv, tables;
-  const int32_t* q_seg;   // [B][Sq]
-  const int32_t* kv_seg;  // [B][Skv]
+  const int32_t* q_seg;      // [B][Sq]
+  const int32_t* kv_seg;     // [B][Skv]
+  const int32_t* seg_range;  // [B][Sq][2] from the mask-info
+  const int32_t* seg_flags;  // bit 0: kv ids not sorted
   // scores
   int32_t score;     // bsm_score
   float scale_log2;  // softmax: scale * log2(e)
@@ -53,11 +64,17 @@ struct FwdParams {
   uint16_t* out;  // bf16 bits
   int64_t o_sb, o_sh, o_ss;
   float* lse;
+  int32_t* unit_counter;  // workspace: next work unit (zeroed per launch)
+  uint16_t* lists;        // workspace: [grid][kListBufs][kMaxKvTiles]
   uint64_t timeout_ns;
+  // optional event trace (records of 16 bytes, cap per CTA), else null
+  void* trace;
+  uint32_t trace_cap;
 };
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream);
+int fwd_grid_size(const FwdParams& p, int num_sms);
 cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               int num_sms, cudaStream_t stream);

@@ -5,12 +5,18 @@
 // next-block table (splash notes section 21: an empty step points at the
 // next nonzero block) plus per-row CSR lists of the nonzero blocks.
 //
-// Three launches:
+// Launches:
+//   0. (segment ids only) segment ranges: for every query row, the first and
+//      last key whose id equals the row's (binary search; exact when each kv
+//      id row is non-decreasing, as for packed sequences), and a flag set if
+//      some kv id row is not sorted.
 //   1. classify: one CTA per (table, q-block row).  Causal/local blocks are
-//      classified exactly from the range of q - k over the block; blocks
-//      that also carry a segment mask are decided from the min/max of the
-//      segment ids when that settles it, else by scanning every element.
-//      Writes block_mask, data_next and the row's nonzero count.
+//      classified exactly from the range of q - k over the block.  With
+//      segment ids and sorted kv ids, every row's visible keys form one
+//      interval, so a block is classified from its rows' intervals; with
+//      unsorted ids the min/max of the ids settle most blocks and the rest
+//      are scanned element by element.  Writes block_mask, data_next and the
+//      row's nonzero count.
 //   2. scan: one CTA turns the counts into CSR row offsets.
 //   3. compact: one CTA per row writes the ascending nonzero list.
 #include <cstdint>
@@ -59,6 +65,36 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
   return v;
 }
 
+// Per query row: [first, last] key index with the row's segment id (binary
+// search in the sorted kv ids), and the "kv ids not sorted" flag.
+__global__ void __launch_bounds__(kMiThreads)
+    mi_segrange_kernel(const MaskInfoParams p) {
+  const int t = blockIdx.y;
+  const int32_t* qs = p.q_seg + static_cast<int64_t>(t) * p.Sq;
+  const int32_t* ks = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k + 1 < p.Skv;
+       k += gridDim.x * blockDim.x) {
+    if (ks[k] > ks[k + 1]) atomicOr(p.seg_flags, 1);
+  }
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= p.Sq) return;
+  const int v = qs[q];
+  int lo = 0, hi = p.Skv;  // first index with ks >= v
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ks[mid] < v) lo = mid + 1; else hi = mid;
+  }
+  int lo2 = lo, hi2 = p.Skv;  // first index with ks > v
+  while (lo2 < hi2) {
+    const int mid = (lo2 + hi2) >> 1;
+    if (ks[mid] <= v) lo2 = mid + 1; else hi2 = mid;
+  }
+  int2 r;
+  r.x = lo;
+  r.y = lo2 - 1;
+  reinterpret_cast<int2*>(p.seg_range)[static_cast<int64_t>(t) * p.Sq + q] = r;
+}
+
 __global__ void __launch_bounds__(kMiThreads)
     mi_classify_kernel(const MaskInfoParams p) {
   extern __shared__ int8_t cls_s[];  // [nk]
@@ -100,12 +136,31 @@ __global__ void __launch_bounds__(kMiThreads)
     }
   }
 
+  const bool ranges = seg && (*p.seg_flags & 1) == 0;
+  const int2* sr = ranges ? reinterpret_cast<const int2*>(p.seg_range) +
+                                static_cast<int64_t>(t) * p.Sq
+                          : nullptr;
+
   // One warp per block (i, j).
   int my_count = 0;
   for (int j = warp; j < p.nk; j += kMiThreads / 32) {
     const BlockRange br = block_range(p, i, j);
     int c = base_class(p, br);
-    if (seg && c != 0) {
+    if (ranges && c != 0) {
+      // each row sees one interval of keys: count it inside the block
+      bool any = false, all = !br.ragged;
+      for (int q = br.r0 + lane; q <= br.r1; q += 32) {
+        int lo = max(br.c0, sr[q].x), hi = min(br.c1, sr[q].y);
+        if (p.flags & BSM_MASK_CAUSAL) hi = min(hi, q);
+        if (p.flags & BSM_MASK_LOCAL) lo = max(lo, q - p.window + 1);
+        const int n = hi >= lo ? hi - lo + 1 : 0;
+        any |= n > 0;
+        all &= n == p.bkv;
+      }
+      any = __any_sync(0xffffffffu, any);
+      all = __all_sync(0xffffffffu, all);
+      c = any ? (all ? 2 : 1) : 0;
+    } else if (seg && c != 0) {
       const int32_t* ks = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
       int kmin = kPosInf, kmax = kNegInf;
       for (int k = br.c0 + lane; k <= br.c1; k += 32) {
@@ -254,9 +309,18 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   if (R == 0) {
     return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t), stream);
   }
+  cudaError_t e;
+  if (p.flags & BSM_MASK_SEGMENT) {
+    e = cudaMemsetAsync(p.seg_flags, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    const int gx = (max(p.Sq, 1) + kMiThreads - 1) / kMiThreads;
+    mi_segrange_kernel<<<dim3(gx, p.tables), kMiThreads, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const size_t smem = static_cast<size_t>(p.nk > 0 ? p.nk : 1);
   mi_classify_kernel<<<dim3(p.nq, p.tables), kMiThreads, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mi_scan_kernel<<<1, 1024, 0, stream>>>(p.row_ptr, R);
   e = cudaGetLastError();

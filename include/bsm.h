@@ -75,6 +75,13 @@ typedef struct bsm_mask_spec {
  *   row_ptr[r]          int32, num_tables*nq + 1 entries, CSR offsets
  *   kv_idx[row_ptr[r]..row_ptr[r+1])  nonzero j of row r, ascending
  *   kv_cls[...]         their classes (1 or 2)
+ *   seg_range[b][q][2]  int32 (SEGMENT only): first and last key index whose
+ *                       segment id equals q's, valid when every kv segment-id
+ *                       row is non-decreasing (packed sequences); first > last
+ *                       when no key has q's id
+ *   seg_flags[0]        int32 (SEGMENT only): bit 0 set if some kv segment-id
+ *                       row is not non-decreasing (then seg_range is unused and
+ *                       segments are compared element by element)
  * kv_idx/kv_cls have capacity num_tables*nq*nk. */
 typedef struct bsm_mask_info {
   uint32_t flags;
@@ -88,6 +95,8 @@ typedef struct bsm_mask_info {
   int32_t* row_ptr;
   int32_t* kv_idx;
   int8_t* kv_cls;
+  int32_t* seg_range;
+  int32_t* seg_flags;
 } bsm_mask_info;
 
 /* Bytes the caller must allocate for bsm_build_mask_info (0 on bad
@@ -137,6 +146,10 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
  *   lse         SOFTMAX: device f32 [B][H][Sq] contiguous, natural-log
  *               logsumexp of the visible scaled logits (-inf for a row that
  *               sees no key), or NULL; POINTWISE: must be NULL
+ *   workspace   device, >= bsm_splash_fwd_workspace_bytes(), 16-aligned:
+ *               the persistent CTAs take work units (batch, head, 256 query
+ *               rows; heaviest rows first) from a counter kept there and
+ *               write the units' KV-tile lists there
  * Rows that see no key get out = 0.  Returns BSM_ERR_UNSUPPORTED for
  * Sq > 262144 or Skv > 262144. */
 bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
@@ -148,7 +161,16 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
                           const bsm_mask_info* info,
                           const int32_t* q_segment_ids,
                           const int32_t* kv_segment_ids, float scale,
-                          int32_t score, void* out, float* lse, void* stream);
+                          int32_t score, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Bytes of the forward's device workspace (about 3 MiB): the work-unit
+ * counter and each CTA's lists of the KV tiles of its next units.  The
+ * counter is zeroed on `stream` before each launch; the launch overwrites
+ * the rest.  Two forward calls that may run at the same time need separate
+ * workspaces. */
+size_t bsm_splash_fwd_workspace_bytes(void);
 
 /* Synchronise `stream` and report whether a kernel of this library gave up
  * on a bounded wait since the last call (then BSM_ERR_DEVICE_TIMEOUT; the
@@ -161,6 +183,20 @@ bsm_status bsm_device_status(void* stream, int32_t* detail);
  * (1e3..1e10), so that the bounded wait must run out.  A later
  * bsm_device_status() then returns BSM_ERR_DEVICE_TIMEOUT. */
 bsm_status bsm_selftest_wait_timeout(int64_t timeout_ns, void* stream);
+
+/* Tracing (diagnostics).  With a non-NULL device buffer, every following
+ * bsm_splash_fwd launch records timestamped events into it: the buffer is
+ * split evenly over the launch's CTAs (see bsm_debug_fwd_grid) into
+ * 16-byte records; a CTA's records 0-1 hold the event counts of its five
+ * roles as uint32 {load, mma, score tile 0, score tile 1, list, 0, 0, 0},
+ * then come five equal regions, one per role, of records {uint64
+ * %globaltimer ns, uint32 role<<28 | event<<24 | tile<<20 | entry, uint32
+ * unit}.  NULL (or bytes too small) switches tracing off.  The buffer stays
+ * owned by the caller; it must outlive the launches. */
+bsm_status bsm_debug_set_trace(void* buffer, size_t bytes);
+
+/* Number of CTAs bsm_splash_fwd launches for these sizes (-1 on error). */
+int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq);
 
 /* Thread-local text of the last error of this thread ("" if none). */
 const char* bsm_last_error(void);

@@ -62,8 +62,10 @@ def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
     T = B if flags & 4 else 1
     nq, nk = -(-Sq // bq), -(-Skv // bkv)
     cells = T * nq * nk
+    seg_rows = B * Sq if flags & 4 else 0
     want = (_align(cells) + _align(4 * cells) + _align(4 * (T * nq + 1))
-            + _align(4 * cells) + _align(cells))
+            + _align(4 * cells) + _align(cells) + _align(8 * seg_rows)
+            + _align(4))
     spec = MaskSpec(flags, 4096 if flags & 2 else 0)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv, bq,
                                    bkv) == want
@@ -111,13 +113,15 @@ def test_build_mask_info_argument_errors(lib):
 
 
 def _fwd(lib, info, B=1, H=2, Hkv=2, Sq=256, Skv=256, D=128, score=0,
-         lse=None, seg=(None, None), strides=None, q=0x10000):
+         lse=None, seg=(None, None), strides=None, q=0x10000, ws=0x70000,
+         wsb=256 + 256 * 3 * 2048 * 2):
     st = strides or (H * Sq * D, Sq * D, D)
     s3 = I64x3(*st)
     kv3 = I64x3(Hkv * Skv * D, Skv * D, D)
     return lib.bsm_splash_fwd(q, 0x20000, 0x30000, s3, kv3, kv3, s3, B, H,
                               Hkv, Sq, Skv, D, ctypes.byref(info), seg[0],
-                              seg[1], 0.125, score, 0x40000, lse, None)
+                              seg[1], 0.125, score, 0x40000, lse, ws, wsb,
+                              None)
 
 
 def _info(flags=1, Sq=256, Skv=256, bq=128, bkv=128, tables=1):
@@ -145,6 +149,10 @@ def test_splash_fwd_argument_errors(lib):
     assert "multiples of 8" in _lib.last_error()
     assert _fwd(lib, info, q=0x10004) == INVALID
     assert _fwd(lib, info, Sq=300000, Skv=300000) == UNSUPPORTED
+    assert _fwd(lib, info, ws=None) == INVALID
+    assert _fwd(lib, info, wsb=8) == INVALID
+    assert "workspace" in _lib.last_error()
+    assert lib.bsm_splash_fwd_workspace_bytes() == 256 + 256 * 3 * 2048 * 2
 
 
 def test_splash_fwd_empty_input_is_a_no_op(lib):

@@ -187,3 +187,39 @@ def test_constant_value_rows_full_size():
     out, _, _ = run_gpu(q, k, v, w.flags, 0, seg, seg, w.scale, SM)
     err = (out - c.float()).abs().max().item()
     assert err <= 2e-2
+
+
+@pytest.mark.parametrize("score", [SM, PW])
+def test_many_repeats_bitwise_identical(score):
+    # The P.V product of a tile and the next Q.K^T into the same TMEM
+    # columns are issued back to back; a reordering would show up as
+    # run-to-run differences.  30 launches with thousands of such pairs each.
+    B, H, S, D = 1, 8, 4096, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=13, sigma=0.5 if score == PW else 1)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    info = bsm.build_mask_info(C, B, S, S, 128, 128, device=dev)
+    ref = None
+    for it in range(30):
+        out = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev) \
+            if score == SM else None
+        bsm.bsm_splash_fwd(qd, kd, vd, info, None, None, 0.09, score, out, lse)
+        if ref is None:
+            ref = (out.clone(), None if lse is None else lse.clone())
+        else:
+            assert torch.equal(out, ref[0]), f"run {it} differs"
+            if lse is not None:
+                assert torch.equal(lse, ref[1]), f"run {it} lse differs"
+    torch.cuda.synchronize()
+    assert bsm.bsm_device_status()[0] == 0
+    rows = [(0, h, r) for h in range(H) for r in (0, 1, 127, 128, 2047, 4095)]
+    got = np.stack([ref[0][b, h, r].float().cpu().numpy() for b, h, r in rows])
+    if score == SM:
+        want, _ = oracle.softmax_attention(q, k, v, C, 0, None, None, 0.09,
+                                           rows=rows)
+        compare_out(got, want, what="repeat")
+    else:
+        want = oracle.pointwise_attention(q, k, v, C, 0, None, None, 0.09,
+                                          rows=rows)
+        compare_out(got, want, pointwise=True, what="repeat")

@@ -78,3 +78,29 @@ def test_empty_kv_mask_info():
     got = _gpu_info(0, 0, None, None, 1, 100, 0, 64, 64)
     assert got["block_mask"].shape == (1, 2, 0)
     np.testing.assert_array_equal(got["row_ptr"], [0, 0, 0])
+
+
+@pytest.mark.parametrize("sorted_ids", [True, False])
+def test_segment_ranges_and_sorted_flag(sorted_ids):
+    B, Sq, Skv = 3, 700, 650
+    if sorted_ids:
+        q_seg = wl.random_segment_ids(B, 800, 5, 120, 3)[:, :Sq].copy()
+        kv_seg = wl.random_segment_ids(B, 800, 5, 120, 3)[:, :Skv].copy()
+    else:
+        rng = np.random.default_rng(5)
+        q_seg = rng.integers(0, 6, size=(B, Sq)).astype(np.int32)
+        kv_seg = rng.integers(0, 6, size=(B, Skv)).astype(np.int32)
+    dev = torch.device("cuda")
+    info = bsm.build_mask_info(bsm.MASK_CAUSAL | bsm.MASK_SEGMENT, B, Sq, Skv,
+                               64, 64, 0, torch.from_numpy(q_seg).to(dev),
+                               torch.from_numpy(kv_seg).to(dev), device=dev)
+    torch.cuda.synchronize()
+    flag = int(info.seg_flags.cpu()[0])
+    assert (flag & 1) == (0 if sorted_ids else 1)
+    if sorted_ids:
+        got = info.seg_range.cpu().numpy()
+        for b in range(B):
+            lo = np.searchsorted(kv_seg[b], q_seg[b], side="left")
+            hi = np.searchsorted(kv_seg[b], q_seg[b], side="right") - 1
+            np.testing.assert_array_equal(got[b, :, 0], lo)
+            np.testing.assert_array_equal(got[b, :, 1], hi)

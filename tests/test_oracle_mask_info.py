@@ -229,3 +229,21 @@ def test_segment_generator_recipe():
         assert np.all(lens[:-1] >= 256) and np.all(lens[:-1] <= 2048)
         assert 1 <= lens[-1] <= 2048
     np.testing.assert_array_equal(seg, wl.make_segment_ids(w))
+
+
+@pytest.mark.parametrize("flags,window", [(1, 0), (3, 300), (5, 0), (4, 0),
+                                          (7, 100), (0, 0), (2, 50)])
+def test_host_flop_count_matches_oracle_pair_count(flags, window):
+    # the benchmark's closed-form pair count (host logic) against the
+    # oracle's element-by-element count
+    from block_sparse_masked_build_gb300 import flops
+    B, S = 2, 900
+    seg = wl.random_segment_ids(B, S, 10, 250, 4)
+    sq = seg if flags & 4 else None
+    assert flops.visible_pairs(flags, window, B, S, S, sq, sq) == \
+        oracle.visible_pair_count(flags, window, sq, sq, B, S, S)
+    if flags & 4:  # unsorted ids take the row-by-row path
+        rng = np.random.default_rng(1)
+        u = rng.integers(0, 3, size=(B, S)).astype(np.int32)
+        assert flops.visible_pairs(flags, window, B, S, S, u, u) == \
+            oracle.visible_pair_count(flags, window, u, u, B, S, S)
