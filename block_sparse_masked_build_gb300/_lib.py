@@ -78,6 +78,12 @@ def _declare(lib):
         c.POINTER(MaskInfoStruct), c.c_void_p, c.c_void_p, c.c_float,
         c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p, c.c_size_t,
         c.c_void_p]
+    lib.bsm_splash_fwd_noalloc.restype = c.c_int
+    lib.bsm_splash_fwd_noalloc.argtypes = [
+        c.c_void_p, c.c_void_p, c.c_void_p, I64x3, I64x3, I64x3, I64x3,
+        c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+        c.POINTER(MaskInfoStruct), c.c_void_p, c.c_void_p, c.c_float,
+        c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p]
     lib.bsm_splash_fwd_workspace_bytes.restype = c.c_size_t
     lib.bsm_splash_fwd_workspace_bytes.argtypes = []
     lib.bsm_device_status.restype = c.c_int

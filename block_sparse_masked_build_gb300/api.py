@@ -185,6 +185,21 @@ def bsm_splash_fwd(q, k, v, mask_info: MaskInfo, q_segment_ids,
         workspace.numel() * workspace.element_size(), sh))
 
 
+def bsm_splash_fwd_noalloc(q, k, v, mask_info: MaskInfo, q_segment_ids,
+                           kv_segment_ids, scale: float, score: int, out,
+                           lse=None, stream=None) -> None:
+    """bsm_splash_fwd using the library's own device scratch (allocates
+    nothing; calls that overlap on the GPU must not be issued)."""
+    B, H, Sq, D = q.shape
+    H_kv, Skv = k.shape[1], k.shape[2]
+    _check(_lib.lib().bsm_splash_fwd_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides3(q), _strides3(k),
+        _strides3(v), _strides3(out), B, H, H_kv, Sq, Skv, D,
+        ctypes.byref(mask_info.struct), _ptr(q_segment_ids),
+        _ptr(kv_segment_ids), float(scale), int(score), out.data_ptr(),
+        _ptr(lse), _stream_handle(stream)))
+
+
 def bsm_device_status(stream=None) -> tuple[int, list[int]]:
     detail = (ctypes.c_int32 * 4)()
     st = _lib.lib().bsm_device_status(_stream_handle(stream), detail)

@@ -168,6 +168,10 @@ bool aligned16(const void* p) {
 
 }  // namespace
 
+namespace bsm {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace bsm
+
 extern "C" {
 
 size_t bsm_mask_info_bytes(const bsm_mask_spec* spec, int32_t B, int32_t Sq,

@@ -79,6 +79,8 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+// Sets the thread-local text returned by bsm_last_error().
+void set_last_error(const char* msg);
 // Reads and clears the device error record of the forward kernel TU.
 cudaError_t read_device_error(int32_t out[4], cudaStream_t stream);
 

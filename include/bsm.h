@@ -172,6 +172,34 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
  * workspaces. */
 size_t bsm_splash_fwd_workspace_bytes(void);
 
+/* bsm_splash_fwd for callers that cannot allocate device memory (this entry
+ * point has no counterpart in the pages; it is a property of this library).
+ * Plugins handed finished buffers by a host framework, serving engines that
+ * reserve all free HBM up front, and loops that cannot afford cudaMalloc's
+ * implicit synchronisation can call it: it takes the same arguments as
+ * bsm_splash_fwd minus the workspace and allocates nothing.  Its workspace
+ * is a 3 MiB (bsm_splash_fwd_workspace_bytes()) array inside the library's
+ * device image, held by every GPU that loads the library until the process
+ * exits.  Limits: Sq, Skv <= 262144 (else BSM_ERR_UNSUPPORTED), at most 256
+ * CTAs (every supported GPU).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array: the work-unit counter in it is zeroed on `stream` before
+ * each launch, and calls that overlap on the GPU (e.g. on two streams) race
+ * on it and must not be issued. */
+bsm_status bsm_splash_fwd_noalloc(const void* q, const void* k, const void* v,
+                                  const int64_t q_strides[3],
+                                  const int64_t k_strides[3],
+                                  const int64_t v_strides[3],
+                                  const int64_t o_strides[3], int32_t B,
+                                  int32_t H, int32_t H_kv, int32_t Sq,
+                                  int32_t Skv, int32_t D,
+                                  const bsm_mask_info* info,
+                                  const int32_t* q_segment_ids,
+                                  const int32_t* kv_segment_ids, float scale,
+                                  int32_t score, void* out, float* lse,
+                                  void* stream);
+
 /* Synchronise `stream` and report whether a kernel of this library gave up
  * on a bounded wait since the last call (then BSM_ERR_DEVICE_TIMEOUT; the
  * affected outputs are undefined, the CUDA context stays usable).  If
