@@ -230,11 +230,11 @@ def decode_trace(buffer, grid: int):
     (t_ns, role, event, tile, entry, unit), sorted by time."""
     raw = buffer.cpu().numpy().view("<u8").reshape(-1, 2)
     per = raw.shape[0] // grid
-    region = (per - 2) // 5
+    region = (per - 2) // 6
     out = []
     for c in range(grid):
         blk = raw[c * per:(c + 1) * per]
-        counts = blk[0:2].reshape(-1).view("<u4")[:5]
+        counts = blk[0:2].reshape(-1).view("<u4")[:6]
         recs = []
         for r, n in enumerate(counts):
             for i in range(int(n)):

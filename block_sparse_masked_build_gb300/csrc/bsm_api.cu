@@ -399,7 +399,7 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
     const int grid = bsm::fwd_grid_size(p, num_sms);
     if (g_trace_buf != nullptr && grid > 0) {
       const size_t per = g_trace_bytes / 16 / static_cast<size_t>(grid);
-      if (per >= 7) {
+      if (per >= 8) {
         p.trace = g_trace_buf;
         p.trace_cap = static_cast<uint32_t>(per - 2);
       }

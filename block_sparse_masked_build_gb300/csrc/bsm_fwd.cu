@@ -7,14 +7,15 @@
 // partial, 2 full).  Empty KV tiles are never loaded (splash notes section
 // 21); the element mask is evaluated on partial tiles only.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warp 10     takes work units from the counter and builds each unit's
 //               KV-tile list, up to two units ahead (three list buffers).
 //   warp 0      issues TMA loads: Q per query tile, K and V tiles through a
 //               ring of shared-memory slots (128-byte swizzle).
-//   warp 1      allocates the 512 TMEM columns and, from one lane, issues the
-//               tcgen05 MMAs: S_t = Q_t K^T (both operands in shared memory)
-//               and O_t += P_t V (P_t read from TMEM, V from shared memory).
+//   warps 1,11  one MMA issuer per query tile (warp 1 also allocates the 512
+//               TMEM columns): from one lane, tcgen05 MMAs S_t = Q_t K^T (both
+//               operands in shared memory) and O_t += P_t V (P_t read from
+//               TMEM, V from shared memory).
 //   warps 2-5   score warpgroup of query tile 0, warps 6-9 of tile 1: one
 //               thread per query row (its TMEM lane).  Softmax: online
 //               max/sum with the correction of the splash notes section 15
@@ -41,7 +42,7 @@ __device__ int g_fwd_error[4];
 
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3, kRoleList = 4;
@@ -70,10 +71,10 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[8], kv_empty[8];  // up to 8 ring slots
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
-  uint32_t trace_n[5];
+  uint32_t trace_n[6];
   ListMeta meta[kListBufs];
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
@@ -87,9 +88,9 @@ __device__ __forceinline__ void record_timeout(int role, int phase) {
 }
 
 // Optional event trace.  CTA c owns records [c*(cap+2), (c+1)*(cap+2)):
-// records 0-1 hold the event counts of the five roles (uint32 each: load,
-// MMA, score tile 0, score tile 1, list), then come five equal per-role
-// regions, each written by one thread with a plain counter.  A record is
+// records 0-1 hold the event counts of the six recording threads (uint32
+// each: load, MMA tile 0, score tile 0, score tile 1, list, MMA tile 1), then
+// come six equal regions, each written by one thread with a plain counter.  A record is
 // {globaltimer ns, role<<28 | event<<24 | tile<<20 | entry, unit}.
 struct TraceRec {
   uint64_t t;
@@ -107,10 +108,10 @@ __device__ __forceinline__ void trace(const FwdParams& p, Bars* bars,
                                       uint32_t entry, uint32_t unit) {
   if (p.trace == nullptr) return;
   const uint32_t slot = role == kRoleScore ? 2 + tile
-                        : role == kRoleMma   ? 1
+                        : role == kRoleMma   ? (tile == 0 ? 1 : 5)
                         : role == kRoleList  ? 4
                                              : 0;
-  const uint32_t per = p.trace_cap / 5;
+  const uint32_t per = p.trace_cap / 6;
   const uint32_t i = bars->trace_n[slot]++;
   if (i < per) {
     TraceRec* r = reinterpret_cast<TraceRec*>(p.trace) +
@@ -333,37 +334,49 @@ __device__ __forceinline__ void load_role(const FwdParams& p,
   }
 }
 
+// MMA issuer of query tile t: one lane of warp 1 (tile 0) or warp 11
+// (tile 1).  The two issuers share the K/V ring: every slot is released by
+// both (kv_empty counts two arrivals), and an issuer whose tile skips an
+// entry still waits for that slot to be filled before releasing it, so the
+// two never drift more than one ring cycle apart.
 template <int D>
 __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
                                          Bars* bars, const uint16_t* lists,
-                                         uint32_t tmem) {
+                                         uint32_t tmem, const int t) {
   using C = Cfg<D>;
   volatile int* abort_flag = &bars->abort;
   constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, true);
+  constexpr uint32_t kTileUnits = C::kTileBytes >> 4;
   // Descriptors of the tile bases; a K-step only adds to the start-address
   // field (16-byte units), which never carries into the upper fields.
-  const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+  const uint64_t dq =
+      sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024) + t * kTileUnits;
   const uint64_t dkv0 = sdesc_sw128(smem_u32(smem + C::kOffKV), 16, 1024);
   const uint64_t dv0 =
       sdesc_sw128(smem_u32(smem + C::kOffKV), kTileN * 128, 1024);
-  constexpr uint32_t kTileUnits = C::kTileBytes >> 4;
-  uint32_t kv_it = 0;
-  uint32_t q_it[2] = {0, 0};
-  uint32_t s_cnt[2] = {0, 0};
+  const uint32_t s_acc = tmem + t * 128;        // S_t, and P_t over it
+  const uint32_t o_acc = tmem + 256 + t * 128;  // O_t
+  uint32_t kv_it = 0, q_it = 0, s_cnt = 0;
   bool ok = true;
 
+  auto wait_slot = [&](int& slot) -> bool {
+    slot = kv_it % C::kSlots;
+    const bool r = mbar_wait(&bars->kv_full[slot], (kv_it / C::kSlots) & 1,
+                             abort_flag, p.timeout_ns);
+    ++kv_it;
+    return r;
+  };
   // S_t = Q_t K^T for the K tile in `kslot`.
-  auto issue_s = [&](int t, int kslot) {
-    const uint64_t a = dq0 + t * kTileUnits;
+  auto issue_s = [&](int kslot) {
     const uint64_t b = dkv0 + kslot * kTileUnits;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
-      mma_ss(tmem + t * 128, a + off, b + off, idesc_s, k > 0 ? 1u : 0u);
+      mma_ss(s_acc, dq + off, b + off, idesc_s, k > 0 ? 1u : 0u);
     }
     mma_commit(&bars->s_full[t]);
-    ++s_cnt[t];
+    ++s_cnt;
   };
 
   for (int ui = 0; ok; ++ui) {
@@ -378,128 +391,95 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
     if (mt.unit < 0) break;
     const int unit = mt.unit;
     const uint16_t* list = lists + buf * kMaxKvTiles;
-    trace(p, bars, kRoleMma, kEvMmaUnit, 0, mt.n, unit);
-    bool q_ready[2] = {false, false};
-    bool first_pv[2] = {true, true};
-    bool s_ahead[2] = {false, false};  // S_t of the current entry already issued
-    int kslot_next = -1;               // K slot of entry e+1 if already waited
+    const int shift = t == 0 ? 2 : 0;
+    trace(p, bars, kRoleMma, kEvMmaUnit, t, mt.n, unit);
+    bool q_ready = false, first_pv = true;
+    bool s_ahead = false;  // S_t of the current entry already issued
+    int kslot_ahead = -1;  // K slot of the current entry if waited ahead
     uint32_t nxt = mt.n > 0 ? list[0] : 0u;  // list entries are read one ahead
     for (int e = 0; e < mt.n && ok; ++e) {
-      const uint32_t ent = nxt;
-      const bool use[2] = {((ent >> 2) & 3u) != 0, (ent & 3u) != 0};
+      const bool use = ((nxt >> shift) & 3u) != 0;
       nxt = (e + 1 < mt.n) ? list[e + 1] : 0u;
-      const bool use_next[2] = {((nxt >> 2) & 3u) != 0, (nxt & 3u) != 0};
-      // ---- K of this entry, and S_t for the tiles not issued ahead
-      int kslot = kslot_next;
-      if (kslot < 0) {
-        kslot = kv_it % C::kSlots;
-        ok = mbar_wait(&bars->kv_full[kslot], (kv_it / C::kSlots) & 1,
-                       abort_flag, p.timeout_ns);
-        if (!ok) {
-          record_timeout(kRoleMma, 2);
-          break;
-        }
-        ++kv_it;
-        trace(p, bars, kRoleMma, kEvKReady, 0, e, unit);
+      const bool use_next = (e + 1 < mt.n) && ((nxt >> shift) & 3u) != 0;
+      // ---- K of this entry
+      int kslot = kslot_ahead;
+      if (kslot < 0 && !(ok = wait_slot(kslot))) {
+        record_timeout(kRoleMma, 2);
+        break;
       }
-      kslot_next = -1;
-      tc_fence_after();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!use[t] || s_ahead[t] || !ok) continue;
-        if (!q_ready[t]) {
-          ok = mbar_wait(&bars->q_full[t], q_it[t] & 1, abort_flag,
-                         p.timeout_ns);
-          q_ready[t] = true;
-          if (!ok) {
+      kslot_ahead = -1;
+      if (use && !s_ahead) {
+        if (!q_ready) {
+          q_ready = true;
+          if (!(ok = mbar_wait(&bars->q_full[t], q_it & 1, abort_flag,
+                               p.timeout_ns))) {
             record_timeout(kRoleMma, 1);
             break;
           }
-          tc_fence_after();
         }
-        issue_s(t, kslot);
+        tc_fence_after();
+        issue_s(kslot);
         trace(p, bars, kRoleMma, kEvSIssued, t, e, unit);
       }
-      if (!ok) break;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (use[t] && e == mt.last_t[t]) {  // Q_t of this unit not needed
-          mma_commit(&bars->q_empty[t]);
-          ++q_it[t];
-        }
+      if (use && e == mt.last_t[t]) {  // Q_t of this unit no longer needed
+        mma_commit(&bars->q_empty[t]);
+        ++q_it;
       }
-      // every S MMA that reads this K tile has been issued
-      mma_commit(&bars->kv_empty[kslot]);
-      // ---- V of this entry; O_t += P_t V, then S_t of the next entry
-      const int vslot = kv_it % C::kSlots;
-      ok = mbar_wait(&bars->kv_full[vslot], (kv_it / C::kSlots) & 1,
-                     abort_flag, p.timeout_ns);
-      if (!ok) {
+      // release the K slot once the S MMA that read it has completed
+      if (use) mma_commit(&bars->kv_empty[kslot]);
+      else mbar_arrive(&bars->kv_empty[kslot]);
+      // ---- V of this entry: O_t += P_t V, then S_t of the next entry
+      int vslot;
+      if (!(ok = wait_slot(vslot))) {
         record_timeout(kRoleMma, 4);
         break;
       }
-      ++kv_it;
-      trace(p, bars, kRoleMma, kEvVReady, 0, e, unit);
-      s_ahead[0] = s_ahead[1] = false;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!use[t] || !ok) continue;
-        ok = mbar_wait(&bars->p_full[t], (s_cnt[t] - 1) & 1, abort_flag,
+      s_ahead = false;
+      if (!use) {
+        mbar_arrive(&bars->kv_empty[vslot]);
+        continue;
+      }
+      ok = mbar_wait(&bars->p_full[t], (s_cnt - 1) & 1, abort_flag,
+                     p.timeout_ns);
+      if (ok && first_pv)
+        ok = mbar_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
                        p.timeout_ns);
-        if (ok && first_pv[t])
-          ok = mbar_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
-                         p.timeout_ns);
-        if (!ok) {
-          record_timeout(kRoleMma, 5);
+      if (!ok) {
+        record_timeout(kRoleMma, 5);
+        break;
+      }
+      trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
+      tc_fence_after();
+      const uint64_t b = dv0 + vslot * kTileUnits;
+      mma_ts(o_acc, s_acc, b, idesc_o, first_pv ? 0u : 1u);
+#pragma unroll
+      for (int kk = 1; kk < kTileN / 16; ++kk)
+        mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
+      first_pv = false;
+      mma_commit(&bars->pv_done[t]);
+      trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
+      // S_t of the next entry goes right behind this P.V.  It overwrites the
+      // TMEM columns the P.V just read: tcgen05.mma instructions of one
+      // thread run in the order they were issued.
+      if (use_next) {
+        if (!(ok = wait_slot(kslot_ahead))) {
+          record_timeout(kRoleMma, 2);
           break;
         }
-        trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
         tc_fence_after();
-        const uint64_t b = dv0 + vslot * kTileUnits;
-        const uint32_t o_acc = tmem + 256 + t * 128;
-        const uint32_t p_tm = tmem + t * 128;
-        if (first_pv[t]) {
-          mma_ts(o_acc, p_tm, b, idesc_o, 0u);
-        } else {
-          mma_ts(o_acc, p_tm, b, idesc_o, 1u);
-        }
-#pragma unroll
-        for (int kk = 1; kk < kTileN / 16; ++kk)
-          mma_ts(o_acc, p_tm + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
-        first_pv[t] = false;
-        mma_commit(&bars->pv_done[t]);
-        trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
-        // S_t of the next entry goes right behind this tile's P.V.  It
-        // overwrites the TMEM columns the P.V just read: tcgen05.mma
-        // instructions of one thread run in the order they were issued.
-        if (use_next[t]) {
-          if (kslot_next < 0) {
-            kslot_next = kv_it % C::kSlots;
-            ok = mbar_wait(&bars->kv_full[kslot_next],
-                           (kv_it / C::kSlots) & 1, abort_flag, p.timeout_ns);
-            if (!ok) {
-              record_timeout(kRoleMma, 2);
-              break;
-            }
-            ++kv_it;
-            trace(p, bars, kRoleMma, kEvKReady, 0, e + 1, unit);
-            tc_fence_after();
-          }
-          issue_s(t, kslot_next);
-          s_ahead[t] = true;
-          trace(p, bars, kRoleMma, kEvSIssued, t, e + 1, unit);
-        }
+        issue_s(kslot_ahead);
+        s_ahead = true;
+        trace(p, bars, kRoleMma, kEvSIssued, t, e + 1, unit);
       }
-      if (!ok) break;
       mma_commit(&bars->kv_empty[vslot]);
     }
     if (!ok) break;
-    trace(p, bars, kRoleMma, kEvMmaLastPv, 0, mt.n, unit);
+    trace(p, bars, kRoleMma, kEvMmaLastPv, t, mt.n, unit);
     mbar_arrive(&bars->list_free[buf]);
   }
   // Drain: every MMA issued above has completed once this arrives.
-  mma_commit(&bars->mma_done);
-  if (!mbar_wait(&bars->mma_done, 0, abort_flag, p.timeout_ns) && ok)
+  mma_commit(&bars->mma_done[t]);
+  if (!mbar_wait(&bars->mma_done[t], 0, abort_flag, p.timeout_ns) && ok)
     record_timeout(kRoleMma, 6);
 }
 
@@ -785,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kListBufs; ++i) {
       mbar_init(&bars->list_full[i], 1);
-      mbar_init(&bars->list_free[i], 2 + 2 * kTileM);  // load, MMA, score
+      mbar_init(&bars->list_free[i], 3 + 2 * kTileM);  // load, 2 MMA, score
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -797,11 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->kv_empty[i], 2);  // both MMA issuers
     }
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done[0], 1);
+    mbar_init(&bars->mma_done[1], 1);
     bars->abort = 0;
-    for (int i = 0; i < 5; ++i) bars->trace_n[i] = 0;
+    for (int i = 0; i < 6; ++i) bars->trace_n[i] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -820,8 +801,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_role<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, lists);
   } else if (warp == 10) {
     list_role(p, bars, lists);
-  } else if (warp == 1) {
-    if ((threadIdx.x % 32) == 0) mma_role<D>(p, smem, bars, lists, tmem);
+  } else if (warp == 1 || warp == 11) {
+    if ((threadIdx.x % 32) == 0)
+      mma_role<D>(p, smem, bars, lists, tmem, warp == 1 ? 0 : 1);
     __syncwarp();
   } else {
     score_role<D, SCORE>(p, bars, lists, tmem);
@@ -835,8 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* hdr = reinterpret_cast<uint32_t*>(
         reinterpret_cast<TraceRec*>(p.trace) +
         static_cast<size_t>(blockIdx.x) * (p.trace_cap + 2));
-    const uint32_t per = p.trace_cap / 5;
-    for (int i = 0; i < 8; ++i) hdr[i] = i < 5 ? min(bars->trace_n[i], per) : 0;
+    const uint32_t per = p.trace_cap / 6;
+    for (int i = 0; i < 8; ++i) hdr[i] = i < 6 ? min(bars->trace_n[i], per) : 0;
   }
 }
 

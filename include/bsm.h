@@ -215,12 +215,12 @@ bsm_status bsm_selftest_wait_timeout(int64_t timeout_ns, void* stream);
 /* Tracing (diagnostics).  With a non-NULL device buffer, every following
  * bsm_splash_fwd launch records timestamped events into it: the buffer is
  * split evenly over the launch's CTAs (see bsm_debug_fwd_grid) into
- * 16-byte records; a CTA's records 0-1 hold the event counts of its five
- * roles as uint32 {load, mma, score tile 0, score tile 1, list, 0, 0, 0},
- * then come five equal regions, one per role, of records {uint64
- * %globaltimer ns, uint32 role<<28 | event<<24 | tile<<20 | entry, uint32
- * unit}.  NULL (or bytes too small) switches tracing off.  The buffer stays
- * owned by the caller; it must outlive the launches. */
+ * 16-byte records; a CTA's records 0-1 hold the event counts of its six
+ * recording threads as uint32 {load, mma tile 0, score tile 0, score tile 1,
+ * list, mma tile 1, 0, 0}, then come six equal regions, one per thread, of
+ * records {uint64 %globaltimer ns, uint32 role<<28 | event<<24 | tile<<20 |
+ * entry, uint32 unit}.  NULL (or bytes too small) switches tracing off.  The
+ * buffer stays owned by the caller; it must outlive the launches. */
 bsm_status bsm_debug_set_trace(void* buffer, size_t bytes);
 
 /* Number of CTAs bsm_splash_fwd launches for these sizes (-1 on error). */
