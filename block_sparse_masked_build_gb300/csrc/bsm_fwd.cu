@@ -334,16 +334,19 @@ __device__ __forceinline__ void load_role(const FwdParams& p,
   }
 }
 
-// MMA issuer of query tile t: one lane of warp 1 (tile 0) or warp 11
-// (tile 1).  The two issuers share the K/V ring: every slot is released by
-// both (kv_empty counts two arrivals), and an issuer whose tile skips an
-// entry still waits for that slot to be filled before releasing it, so the
-// two never drift more than one ring cycle apart.
+// MMA issuer of query tile t: warp 1 (tile 0) or warp 11 (tile 1).  The
+// whole warp runs the loop and waits together; lane 0 issues the MMAs and
+// the commits (a commit tracks the MMAs of the thread that issues it).  The
+// two issuers share the K/V ring: every slot is released by both (kv_empty
+// counts two arrivals), and an issuer whose tile skips an entry still waits
+// for that slot to be filled before releasing it, so the two never drift
+// more than one ring cycle apart.
 template <int D>
 __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
                                          Bars* bars, const uint16_t* lists,
                                          uint32_t tmem, const int t) {
   using C = Cfg<D>;
+  const bool leader = (threadIdx.x % 32) == 0;
   volatile int* abort_flag = &bars->abort;
   constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, D, true);
@@ -362,12 +365,12 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
 
   auto wait_slot = [&](int& slot) -> bool {
     slot = kv_it % C::kSlots;
-    const bool r = mbar_wait(&bars->kv_full[slot], (kv_it / C::kSlots) & 1,
+    const bool r = warp_wait(&bars->kv_full[slot], (kv_it / C::kSlots) & 1,
                              abort_flag, p.timeout_ns);
     ++kv_it;
     return r;
   };
-  // S_t = Q_t K^T for the K tile in `kslot`.
+  // S_t = Q_t K^T for the K tile in `kslot` (lane 0).
   auto issue_s = [&](int kslot) {
     const uint64_t b = dkv0 + kslot * kTileUnits;
 #pragma unroll
@@ -376,15 +379,17 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
       mma_ss(s_acc, dq + off, b + off, idesc_s, k > 0 ? 1u : 0u);
     }
     mma_commit(&bars->s_full[t]);
-    ++s_cnt;
+  };
+  auto fail = [&](int where) {
+    if (leader) record_timeout(kRoleMma, where);
   };
 
   for (int ui = 0; ok; ++ui) {
     const int buf = ui % kListBufs;
-    ok = mbar_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
+    ok = warp_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
                    p.timeout_ns);
     if (!ok) {
-      record_timeout(kRoleMma, 0);
+      fail(0);
       break;
     }
     const ListMeta mt = bars->meta[buf];
@@ -392,7 +397,7 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
     const int unit = mt.unit;
     const uint16_t* list = lists + buf * kMaxKvTiles;
     const int shift = t == 0 ? 2 : 0;
-    trace(p, bars, kRoleMma, kEvMmaUnit, t, mt.n, unit);
+    if (leader) trace(p, bars, kRoleMma, kEvMmaUnit, t, mt.n, unit);
     bool q_ready = false, first_pv = true;
     bool s_ahead = false;  // S_t of the current entry already issued
     int kslot_ahead = -1;  // K slot of the current entry if waited ahead
@@ -404,83 +409,101 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
       // ---- K of this entry
       int kslot = kslot_ahead;
       if (kslot < 0 && !(ok = wait_slot(kslot))) {
-        record_timeout(kRoleMma, 2);
+        fail(2);
         break;
       }
       kslot_ahead = -1;
       if (use && !s_ahead) {
         if (!q_ready) {
           q_ready = true;
-          if (!(ok = mbar_wait(&bars->q_full[t], q_it & 1, abort_flag,
+          if (!(ok = warp_wait(&bars->q_full[t], q_it & 1, abort_flag,
                                p.timeout_ns))) {
-            record_timeout(kRoleMma, 1);
+            fail(1);
             break;
           }
         }
-        tc_fence_after();
-        issue_s(kslot);
-        trace(p, bars, kRoleMma, kEvSIssued, t, e, unit);
+        if (leader) {
+          tc_fence_after();
+          issue_s(kslot);
+          trace(p, bars, kRoleMma, kEvSIssued, t, e, unit);
+        }
+        ++s_cnt;
       }
-      if (use && e == mt.last_t[t]) {  // Q_t of this unit no longer needed
-        mma_commit(&bars->q_empty[t]);
-        ++q_it;
+      if (leader) {
+        if (use && e == mt.last_t[t])  // Q_t of this unit no longer needed
+          mma_commit(&bars->q_empty[t]);
+        // release the K slot once the S MMA that read it has completed
+        if (use) mma_commit(&bars->kv_empty[kslot]);
+        else mbar_arrive(&bars->kv_empty[kslot]);
       }
-      // release the K slot once the S MMA that read it has completed
-      if (use) mma_commit(&bars->kv_empty[kslot]);
-      else mbar_arrive(&bars->kv_empty[kslot]);
+      if (use && e == mt.last_t[t]) ++q_it;
+      __syncwarp();
       // ---- V of this entry: O_t += P_t V, then S_t of the next entry
       int vslot;
       if (!(ok = wait_slot(vslot))) {
-        record_timeout(kRoleMma, 4);
+        fail(4);
         break;
       }
       s_ahead = false;
       if (!use) {
-        mbar_arrive(&bars->kv_empty[vslot]);
+        if (leader) mbar_arrive(&bars->kv_empty[vslot]);
+        __syncwarp();
         continue;
       }
-      ok = mbar_wait(&bars->p_full[t], (s_cnt - 1) & 1, abort_flag,
+      ok = warp_wait(&bars->p_full[t], (s_cnt - 1) & 1, abort_flag,
                      p.timeout_ns);
       if (ok && first_pv)
-        ok = mbar_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
+        ok = warp_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
                        p.timeout_ns);
       if (!ok) {
-        record_timeout(kRoleMma, 5);
+        fail(5);
         break;
       }
-      trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
-      tc_fence_after();
-      const uint64_t b = dv0 + vslot * kTileUnits;
-      mma_ts(o_acc, s_acc, b, idesc_o, first_pv ? 0u : 1u);
+      if (leader) {
+        trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
+        tc_fence_after();
+        const uint64_t b = dv0 + vslot * kTileUnits;
+        mma_ts(o_acc, s_acc, b, idesc_o, first_pv ? 0u : 1u);
 #pragma unroll
-      for (int kk = 1; kk < kTileN / 16; ++kk)
-        mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
+        for (int kk = 1; kk < kTileN / 16; ++kk)
+          mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
+        mma_commit(&bars->pv_done[t]);
+        trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
+      }
       first_pv = false;
-      mma_commit(&bars->pv_done[t]);
-      trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
       // S_t of the next entry goes right behind this P.V.  It overwrites the
       // TMEM columns the P.V just read: tcgen05.mma instructions of one
       // thread run in the order they were issued.
       if (use_next) {
         if (!(ok = wait_slot(kslot_ahead))) {
-          record_timeout(kRoleMma, 2);
+          fail(2);
           break;
         }
-        tc_fence_after();
-        issue_s(kslot_ahead);
+        if (leader) {
+          tc_fence_after();
+          issue_s(kslot_ahead);
+          trace(p, bars, kRoleMma, kEvSIssued, t, e + 1, unit);
+        }
+        ++s_cnt;
         s_ahead = true;
-        trace(p, bars, kRoleMma, kEvSIssued, t, e + 1, unit);
       }
-      mma_commit(&bars->kv_empty[vslot]);
+      if (leader) mma_commit(&bars->kv_empty[vslot]);
+      __syncwarp();
     }
     if (!ok) break;
-    trace(p, bars, kRoleMma, kEvMmaLastPv, t, mt.n, unit);
-    mbar_arrive(&bars->list_free[buf]);
+    if (leader) {
+      trace(p, bars, kRoleMma, kEvMmaLastPv, t, mt.n, unit);
+      mbar_arrive(&bars->list_free[buf]);
+    }
+    __syncwarp();
   }
   // Drain: every MMA issued above has completed once this arrives.
-  mma_commit(&bars->mma_done[t]);
-  if (!mbar_wait(&bars->mma_done[t], 0, abort_flag, p.timeout_ns) && ok)
-    record_timeout(kRoleMma, 6);
+  if (leader) {
+    mma_commit(&bars->mma_done[t]);
+    if (!mbar_wait(&bars->mma_done[t], 0, abort_flag, p.timeout_ns) && ok)
+      record_timeout(kRoleMma, 6);
+  }
+  __syncwarp();
 }
 
 // "Same segment" bits of the 128 keys of a tile for one row (unsorted
@@ -802,9 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 10) {
     list_role(p, bars, lists);
   } else if (warp == 1 || warp == 11) {
-    if ((threadIdx.x % 32) == 0)
-      mma_role<D>(p, smem, bars, lists, tmem, warp == 1 ? 0 : 1);
-    __syncwarp();
+    mma_role<D>(p, smem, bars, lists, tmem, warp == 1 ? 0 : 1);
   } else {
     score_role<D, SCORE>(p, bars, lists, tmem);
   }
