@@ -51,6 +51,8 @@ class MaskInfoStruct(ctypes.Structure):
         ("kv_cls", ctypes.c_void_p),
         ("seg_range", ctypes.c_void_p),
         ("seg_flags", ctypes.c_void_p),
+        ("num_super", ctypes.c_int32),
+        ("super_order", ctypes.c_void_p),
     ]
 
 

@@ -119,6 +119,16 @@ class MaskInfo:
     def seg_flags(self) -> torch.Tensor:
         return self._view(self.struct.seg_flags, torch.int32, 1)
 
+    @property
+    def super_order(self):
+        """[num_tables * num_super] longest-first (table, 256-row super-tile)
+        pairs as table * num_super + super_tile, or None when not built."""
+        s = self.struct
+        if not s.super_order:
+            return None
+        return self._view(s.super_order, torch.int32,
+                          s.num_tables * s.num_super)
+
     def kv_lists(self) -> tuple[torch.Tensor, torch.Tensor]:
         """(kv_idx, kv_cls) trimmed to row_ptr[-1] entries (synchronises)."""
         s = self.struct

@@ -33,11 +33,17 @@ bool is_block_size(int32_t b) {
 }
 
 struct MiLayout {
-  size_t off_bm, off_dn, off_rp, off_idx, off_cls, off_sr, off_sf, total;
+  size_t off_bm, off_dn, off_rp, off_idx, off_cls, off_sr, off_sf, off_so,
+      total;
 };
 
 // seg_rows = B * Sq with segment ids, else 0.
-MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows) {
+int64_t super_pairs(int64_t tables, int64_t Sq) {
+  return tables * ((Sq + bsm::kUnitRows - 1) / bsm::kUnitRows);
+}
+
+MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows,
+                   int64_t pairs) {
   const size_t cells = static_cast<size_t>(tables * nq * nk);
   const size_t rows = static_cast<size_t>(tables * nq);
   MiLayout L;
@@ -56,6 +62,9 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows) {
   o = align_up(o + static_cast<size_t>(seg_rows) * 8, 256);
   L.off_sf = o;
   o = align_up(o + 4, 256);
+  L.off_so = o;
+  if (pairs <= bsm::kMaxSuperOrder)
+    o = align_up(o + static_cast<size_t>(pairs) * 4, 256);
   L.total = o;
   return L;
 }
@@ -181,7 +190,8 @@ size_t bsm_mask_info_bytes(const bsm_mask_spec* spec, int32_t B, int32_t Sq,
   const int64_t tables = seg ? B : 1;
   const int64_t nq = (Sq + block_q - 1) / block_q;
   const int64_t nk = (Skv + block_kv - 1) / block_kv;
-  return mi_layout(tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0)
+  return mi_layout(tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0,
+                   super_pairs(tables, Sq))
       .total;
 }
 
@@ -209,8 +219,9 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   const int64_t nk = (Skv + block_kv - 1) / block_kv;
   if (tables > 65535)
     return fail(BSM_ERR_UNSUPPORTED, "too many mask tables");
-  const MiLayout L =
-      mi_layout(tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0);
+  const int64_t pairs = super_pairs(tables, Sq);
+  const MiLayout L = mi_layout(
+      tables, nq, nk, seg ? static_cast<int64_t>(B) * Sq : 0, pairs);
   if (buffer == nullptr) return fail(BSM_ERR_INVALID_ARG, "buffer is NULL");
   if ((reinterpret_cast<uintptr_t>(buffer) & 255u) != 0)
     return fail(BSM_ERR_INVALID_ARG, "buffer must be 256-byte aligned");
@@ -239,6 +250,10 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   mi.kv_cls = reinterpret_cast<int8_t*>(base + L.off_cls);
   mi.seg_range = reinterpret_cast<int32_t*>(base + L.off_sr);
   mi.seg_flags = reinterpret_cast<int32_t*>(base + L.off_sf);
+  mi.num_super = static_cast<int32_t>((Sq + bsm::kUnitRows - 1) / bsm::kUnitRows);
+  mi.super_order = pairs <= bsm::kMaxSuperOrder
+                       ? reinterpret_cast<int32_t*>(base + L.off_so)
+                       : nullptr;
 
   bsm::MaskInfoParams p;
   p.flags = mi.flags;
@@ -259,6 +274,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   p.kv_cls = mi.kv_cls;
   p.seg_range = mi.seg_range;
   p.seg_flags = mi.seg_flags;
+  p.n_super = mi.num_super;
+  p.super_order = mi.super_order;
   cudaError_t e =
       bsm::launch_mask_info(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mask-info launch");
@@ -303,7 +320,8 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
                 "mask info was built for another batch size");
   if (!is_block_size(info->block_q) || !is_block_size(info->block_kv) ||
       info->nq != (Sq + info->block_q - 1) / info->block_q ||
-      info->nk != (Skv + info->block_kv - 1) / info->block_kv)
+      info->nk != (Skv + info->block_kv - 1) / info->block_kv ||
+      info->num_super != (Sq + bsm::kUnitRows - 1) / bsm::kUnitRows)
     return fail(BSM_ERR_INVALID_ARG, "inconsistent mask info");
   if (seg && (q_segment_ids == nullptr || kv_segment_ids == nullptr))
     return fail(BSM_ERR_INVALID_ARG,
@@ -378,6 +396,7 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.kv_seg = kv_segment_ids;
   p.seg_range = info->seg_range;
   p.seg_flags = info->seg_flags;
+  p.super_order = info->super_order;
   p.score = score;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale = scale;

@@ -64,6 +64,7 @@ struct ListMeta {
   int n_t[2];     // entries used by query tile t
   int last_t[2];  // index of the last entry used by query tile t (-1: none)
   int unit;
+  int b, h, st;   // the unit's batch row, head and 256-row super-tile
 };
 
 struct Bars {
@@ -136,15 +137,28 @@ struct UnitCoord {
   int b, h, st;
 };
 
+// Work unit u -> (batch, head, super-tile).  Units come in groups that
+// share one (mask table, super-tile) pair: all heads of that batch row with
+// one table per batch row, else all batch rows and heads.  The pairs are
+// taken longest first when the mask info carries that order; otherwise the
+// last super-tiles go first (under a causal mask the last rows see the most
+// keys).
 __device__ __forceinline__ UnitCoord decode_unit(const FwdParams& p, int u) {
-  // Heaviest super-tiles first: under a causal mask the last rows see the
-  // most keys.
-  const int bh_count = p.B * p.H;
+  const int per = p.tables == 1 ? p.B * p.H : p.H;
+  const int rank = u / per, r = u % per;
+  int table, st;
+  if (p.super_order != nullptr) {
+    const int pr = p.super_order[rank];
+    table = pr / p.n_super;
+    st = pr % p.n_super;
+  } else {
+    table = rank % p.tables;
+    st = p.n_super - 1 - rank / p.tables;
+  }
   UnitCoord c;
-  c.st = p.n_super - 1 - u / bh_count;
-  const int bh = u % bh_count;
-  c.b = bh / p.H;
-  c.h = bh % p.H;
+  c.st = st;
+  c.b = p.tables == 1 ? r / p.H : table;
+  c.h = p.tables == 1 ? r % p.H : r;
   return c;
 }
 
@@ -239,6 +253,9 @@ __device__ __forceinline__ bool build_list(const FwdParams& p, Bars* bars,
     mt.last_t[0] = last0;
     mt.last_t[1] = last1;
     mt.unit = unit;
+    mt.b = uc.b;
+    mt.h = uc.h;
+    mt.st = uc.st;
     trace(p, bars, kRoleList, kEvListBuilt, 0, n, unit);
     mbar_arrive(&bars->list_full[buf]);
   }
@@ -281,7 +298,7 @@ __device__ __forceinline__ void load_role(const FwdParams& p,
     if (mt.unit < 0) break;
     const int unit = mt.unit;
     const uint16_t* list = lists + buf * kMaxKvTiles;
-    const UnitCoord uc = decode_unit(p, unit);
+    const UnitCoord uc{mt.b, mt.h, mt.st};
     const int row0 = uc.st * kUnitRows;
     // Q, per query tile that has work in this unit
 #pragma unroll
@@ -578,9 +595,11 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       record_timeout(kRoleScore, 0);
       break;
     }
-    const ListMeta mt = bars->meta[buf];
-    if (mt.unit < 0) break;
-    const UnitCoord uc = decode_unit(p, mt.unit);
+    const int unit = bars->meta[buf].unit;
+    if (unit < 0) break;
+    const int n_ent = bars->meta[buf].n;
+    const UnitCoord uc{bars->meta[buf].b, bars->meta[buf].h,
+                       bars->meta[buf].st};
     const uint16_t* list = lists + buf * kMaxKvTiles;
     const int qrow = uc.st * kUnitRows + t * kTileM + r;
     const bool row_ok = qrow < p.Sq;
@@ -605,7 +624,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
     float m_used = NEG_INF, l_sum = 0.f;
     uint32_t unit_pv = 0;
     bool ok = true;
-    for (int e = 0; e < mt.n; ++e) {
+    for (int e = 0; e < n_ent; ++e) {
       const uint32_t ent = list[e];
       const int cls = t == 0 ? static_cast<int>((ent >> 2) & 3u)
                              : static_cast<int>(ent & 3u);
@@ -621,7 +640,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         break;
       }
       ++s_cnt;
-      if (tracer) trace(p, bars, kRoleScore, kEvSFull, t, e, mt.unit);
+      if (tracer) trace(p, bars, kRoleScore, kEvSFull, t, e, unit);
       tc_fence_after();
       uint32_t sraw[kTileN];
 #pragma unroll
@@ -681,7 +700,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
             record_timeout(kRoleScore, 2);
             break;
           }
-          if (tracer) trace(p, bars, kRoleScore, kEvRescale, t, e, mt.unit);
+          if (tracer) trace(p, bars, kRoleScore, kEvRescale, t, e, unit);
           tc_fence_after();
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
@@ -716,14 +735,14 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
-      if (tracer) trace(p, bars, kRoleScore, kEvPFull, t, e, mt.unit);
+      if (tracer) trace(p, bars, kRoleScore, kEvPFull, t, e, unit);
       ++pv_cnt;
       ++unit_pv;
     }
     if (!ok) break;
 
     // ---- epilogue: out = O / l (softmax) or O (pointwise), bf16
-    if (tracer) trace(p, bars, kRoleScore, kEvEpiBegin, t, 0, mt.unit);
+    if (tracer) trace(p, bars, kRoleScore, kEvEpiBegin, t, 0, unit);
     uint16_t* orow = p.out + static_cast<int64_t>(uc.b) * p.o_sb +
                      static_cast<int64_t>(uc.h) * p.o_sh +
                      static_cast<int64_t>(qrow) * p.o_ss;
@@ -766,7 +785,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
     tc_fence_before();
     mbar_arrive(&bars->o_free[t]);
     mbar_arrive(&bars->list_free[buf]);
-    if (tracer) trace(p, bars, kRoleScore, kEvEpiEnd, t, 0, mt.unit);
+    if (tracer) trace(p, bars, kRoleScore, kEvEpiEnd, t, 0, unit);
   }
 }
 

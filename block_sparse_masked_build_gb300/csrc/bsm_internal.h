@@ -21,6 +21,7 @@ constexpr int kMaxKvTiles = kMaxSeq / kTileN;  // list capacity per unit
 // Forward workspace: 256 bytes of counters, then per CTA three unit lists of
 // kMaxKvTiles uint16 entries (up to kMaxCtas CTAs).
 constexpr int kMaxCtas = 256;
+constexpr int kMaxSuperOrder = 8192;  // longest-first table size limit
 constexpr int kListBufs = 3;
 constexpr size_t kListBytes = static_cast<size_t>(kMaxKvTiles) * 2;
 constexpr size_t kFwdWorkspaceBytes =
@@ -39,11 +40,14 @@ struct MaskInfoParams {
   int8_t* kv_cls;
   int32_t* seg_range;  // [tables][Sq][2] (SEGMENT only)
   int32_t* seg_flags;  // [1]: bit 0 = some kv id row is not sorted
+  int32_t n_super;        // ceil(Sq / kUnitRows)
+  int32_t* super_order;   // [tables * n_super] or null
 };
 
 struct FwdParams {
   int32_t B, H, Hkv, Sq, Skv, D;
   int32_t n_super;    // ceil(Sq / 256)
+  const int32_t* super_order;  // longest-first (table, super-tile) or null
   int32_t n_kvtiles;  // ceil(Skv / 128)
   int32_t num_units;  // B * H * n_super
   // mask

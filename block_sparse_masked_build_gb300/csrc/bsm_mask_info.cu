@@ -234,15 +234,23 @@ __global__ void __launch_bounds__(kMiThreads)
   }
 }
 
-// Inclusive scan of row_ptr[1..R] in place (row_ptr[0] = 0): CSR offsets.
-__global__ void __launch_bounds__(1024) mi_scan_kernel(int32_t* row_ptr,
-                                                       int R) {
+// One CTA: inclusive scan of the row counts in row_ptr[1..R] in place
+// (row_ptr[0] = 0), giving the CSR offsets; then, if requested, the order in
+// which the forward should take its 256-row super-tiles: by decreasing work
+// (sum over the super-tile's rows of the nonzero blocks they see), so that
+// the longest units start first and the short ones fill in at the end.
+__global__ void __launch_bounds__(1024) mi_scan_kernel(const MaskInfoParams p) {
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
+  __shared__ unsigned long long wmax_s;
+  __shared__ uint32_t keys[kMaxSuperOrder];
+  int32_t* row_ptr = p.row_ptr;
+  const int R = p.tables * p.nq;
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
     row_ptr[0] = 0;
     carry_s = 0;
+    wmax_s = 0;
   }
   __syncthreads();
   for (int base = 0; base < R; base += blockDim.x) {
@@ -270,6 +278,59 @@ __global__ void __launch_bounds__(1024) mi_scan_kernel(int32_t* row_ptr,
     if (threadIdx.x == blockDim.x - 1) carry_s = carry + warp_sums[31];
     __syncthreads();
   }
+  if (p.super_order == nullptr) return;
+
+  // ---- longest-first order of the (table, super-tile) pairs
+  const int pairs = p.tables * p.n_super;  // <= kMaxSuperOrder
+  auto work = [&](int pr) -> unsigned long long {
+    const int t = pr / p.n_super, st = pr % p.n_super;
+    const int r0 = st * kUnitRows, r1 = min(p.Sq, r0 + kUnitRows);
+    unsigned long long w = 0;
+    for (int i = r0 / p.bq; i <= (r1 - 1) / p.bq; ++i) {
+      const int cnt = row_ptr[t * p.nq + i + 1] - row_ptr[t * p.nq + i];
+      const int rows = min(r1, (i + 1) * p.bq) - max(r0, i * p.bq);
+      w += static_cast<unsigned long long>(cnt) * rows;
+    }
+    return w;
+  };
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x)
+    atomicMax(&wmax_s, work(pr));
+  __syncthreads();
+  const unsigned long long wmax = wmax_s > 0 ? wmax_s : 1;
+  int n2 = 1;
+  while (n2 < pairs) n2 <<= 1;
+  // key: complemented 19-bit work above the complemented 13-bit index, so
+  // an ascending sort gives decreasing work and, among equals, decreasing
+  // index (later rows first, as for a causal mask)
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    uint32_t key = 0xffffffffu;
+    if (i < pairs) {
+      const unsigned long long q = work(i) * 0x7ffffull / wmax;
+      key = (static_cast<uint32_t>(0x7ffffull - q) << 13) |
+            (0x1fffu - static_cast<uint32_t>(i));
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  // bitonic sort of keys[0..n2)
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = keys[i], b = keys[l];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < pairs; i += blockDim.x)
+    p.super_order[i] = static_cast<int32_t>(0x1fffu - (keys[i] & 0x1fffu));
 }
 
 // Ascending list of the nonzero blocks of one row.
@@ -322,7 +383,7 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   mi_classify_kernel<<<dim3(p.nq, p.tables), kMiThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mi_scan_kernel<<<1, 1024, 0, stream>>>(p.row_ptr, R);
+  mi_scan_kernel<<<1, 1024, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);

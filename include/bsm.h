@@ -82,6 +82,17 @@ typedef struct bsm_mask_spec {
  *   seg_flags[0]        int32 (SEGMENT only): bit 0 set if some kv segment-id
  *                       row is not non-decreasing (then seg_range is unused and
  *                       segments are compared element by element)
+ *   super_order[k]      int32, num_tables*num_super entries: the pairs
+ *                       (table t, super-tile s) as t*num_super + s, ordered by
+ *                       decreasing work (query rows times nonzero blocks
+ *                       they see, quantised to 19 bits of the largest),
+ *                       ties by decreasing index.  A super-tile is 256 query
+ *                       rows, the forward's work unit; bsm_splash_fwd hands
+ *                       its units out in this order (longest first).  NULL
+ *                       when num_tables*num_super > 8192 (the forward then
+ *                       takes the last super-tiles first).  Scheduling only:
+ *                       no result depends on it.  No counterpart on the
+ *                       pages, whose grid walks the query blocks in order.
  * kv_idx/kv_cls have capacity num_tables*nq*nk. */
 typedef struct bsm_mask_info {
   uint32_t flags;
@@ -97,6 +108,8 @@ typedef struct bsm_mask_info {
   int8_t* kv_cls;
   int32_t* seg_range;
   int32_t* seg_flags;
+  int32_t num_super; /* ceil(Sq / 256) */
+  int32_t* super_order;
 } bsm_mask_info;
 
 /* Bytes the caller must allocate for bsm_build_mask_info (0 on bad

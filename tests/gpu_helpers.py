@@ -26,8 +26,10 @@ PW_MEAN_REL = 2.0 ** -8
 
 
 def run_gpu(q, k, v, flags, window, q_seg, kv_seg, scale, score,
-            block_q=128, block_kv=128, layout="bhsd"):
-    """Run mask-info build + forward on the GPU; returns CPU out, lse, info."""
+            block_q=128, block_kv=128, layout="bhsd", longest_first=True):
+    """Run mask-info build + forward on the GPU; returns CPU out, lse, info.
+    longest_first=False drops the mask info's unit order, so the forward
+    takes its fallback schedule."""
     dev = torch.device("cuda")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     if layout == "bshd":  # store as [B, S, H, D] and pass transposed views
@@ -48,6 +50,8 @@ def run_gpu(q, k, v, flags, window, q_seg, kv_seg, scale, score,
     if score == bsm.SCORE_SOFTMAX:
         lse = torch.full((B, H, Sq), float("nan"), dtype=torch.float32,
                          device=dev)
+    if not longest_first:
+        info.struct.super_order = None
     bsm.bsm_splash_fwd(qd, kd, vd, info, qs, ks, scale, score, out, lse)
     torch.cuda.synchronize()
     st, detail = bsm.bsm_device_status()

@@ -57,15 +57,16 @@ def _align(x, a=256):
 @pytest.mark.parametrize("flags,B,Sq,Skv,bq,bkv", [
     (1, 4, 2048, 2048, 128, 128), (5, 2, 8192, 8192, 128, 128),
     (3, 1, 32768, 32768, 128, 128), (1, 1, 256, 256, 64, 64),
-    (4, 3, 700, 300, 64, 32)])
+    (4, 3, 700, 300, 64, 32), (4, 9, 262144, 256, 512, 512)])
 def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
     T = B if flags & 4 else 1
     nq, nk = -(-Sq // bq), -(-Skv // bkv)
     cells = T * nq * nk
     seg_rows = B * Sq if flags & 4 else 0
+    pairs = T * -(-Sq // 256)  # (table, 256-row super-tile) pairs
     want = (_align(cells) + _align(4 * cells) + _align(4 * (T * nq + 1))
             + _align(4 * cells) + _align(cells) + _align(8 * seg_rows)
-            + _align(4))
+            + _align(4) + (_align(4 * pairs) if pairs <= 8192 else 0))
     spec = MaskSpec(flags, 4096 if flags & 2 else 0)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv, bq,
                                    bkv) == want
@@ -129,6 +130,7 @@ def _info(flags=1, Sq=256, Skv=256, bq=128, bkv=128, tables=1):
     i.flags, i.window, i.num_tables = flags, 0, tables
     i.Sq, i.Skv, i.block_q, i.block_kv = Sq, Skv, bq, bkv
     i.nq, i.nk = -(-Sq // bq), -(-Skv // bkv)
+    i.num_super = -(-Sq // 256)
     i.block_mask = 0x50000
     return i
 

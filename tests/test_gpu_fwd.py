@@ -143,6 +143,19 @@ def test_block_size_independence(score):
             assert torch.equal(l, outs[0][1])
 
 
+@pytest.mark.parametrize("flags", [C | SG, C])
+def test_unit_order_does_not_change_results(flags):
+    # longest-first and fallback schedules give bit-identical outputs
+    B, H, S, D = 2, 3, 1000, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=13)
+    seg = wl.random_segment_ids(B, S, 40, 400, 14) if flags & SG else None
+    a, la, ia = run_gpu(q, k, v, flags, 0, seg, seg, 0.1, SM)
+    assert ia.super_order is not None
+    b, lb, _ = run_gpu(q, k, v, flags, 0, seg, seg, 0.1, SM,
+                       longest_first=False)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
 def test_repeated_calls_are_deterministic():
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = _qkv(B, H, H, S, S, D, seed=12)

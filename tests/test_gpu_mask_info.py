@@ -25,7 +25,36 @@ def _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv):
         "row_ptr": info.row_ptr.cpu().numpy(),
         "kv_idx": idx.cpu().numpy(),
         "kv_cls": cls.cpu().numpy(),
+        "super_order": (None if info.super_order is None
+                        else info.super_order.cpu().numpy()),
+        "num_super": info.struct.num_super,
     }
+
+
+def _check_super_order(got, ref, T, nq, bq, Sq):
+    """The forward's longest-first schedule: every (table, 256-row
+    super-tile) pair once, by decreasing work (rows times nonzero blocks,
+    quantised to 19 bits of the largest), ties by decreasing index."""
+    ns = -(-Sq // 256)
+    assert got["num_super"] == ns
+    order = got["super_order"]
+    if T * ns > 8192:
+        assert order is None
+        return
+    assert sorted(order.tolist()) == list(range(T * ns))
+    rp = ref["row_ptr"]
+    work = []
+    for pr in range(T * ns):
+        t, st = divmod(pr, ns)
+        r0, r1 = st * 256, min(Sq, st * 256 + 256)
+        w = 0
+        for i in range(r0 // bq, (r1 - 1) // bq + 1):
+            cnt = int(rp[t * nq + i + 1] - rp[t * nq + i])
+            w += cnt * (min(r1, (i + 1) * bq) - max(r0, i * bq))
+        work.append(w)
+    wmax = max(max(work), 1)
+    keys = [(-(w * 0x7FFFF // wmax), -i) for i, w in enumerate(work)]
+    assert [-k[1] for k in sorted(keys)] == order.tolist()
 
 
 def _assert_same(got, ref):
@@ -42,6 +71,8 @@ def test_workload_mask_info_bit_exact(name):
     got = _gpu_info(w.flags, w.window, seg, seg, w.B, w.Sq, w.Skv_, w.block_q,
                     w.block_kv)
     _assert_same(got, ref)
+    T = w.B if w.flags & 4 else 1
+    _check_super_order(got, ref, T, -(-w.Sq // w.block_q), w.block_q, w.Sq)
 
 
 CASES = []
@@ -72,6 +103,17 @@ def test_random_tiny_mask_info_bit_exact(n, flags, window, bq, bkv, Sq, Skv, B):
     ref = oracle.mask_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv)
     got = _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv)
     _assert_same(got, ref)
+    T = B if flags & 4 else 1
+    _check_super_order(got, ref, T, -(-Sq // bq), bq, Sq)
+
+
+def test_super_order_absent_above_limit():
+    # 9 tables x 1024 super-tiles exceed the 8192-pair table: no order, and
+    # the forward falls back to taking the last super-tiles first
+    B, Sq = 9, 262144
+    seg = np.zeros((B, Sq), np.int32)
+    got = _gpu_info(4, 0, seg, seg, B, Sq, 256, 512, 512)
+    assert got["super_order"] is None and got["num_super"] == 1024
 
 
 def test_empty_kv_mask_info():
