@@ -1,22 +1,24 @@
 // Block-sparse masked attention forward for sm_103a (GB300).
 //
 // One persistent CTA per SM takes work units of (batch, head, 256 query
-// rows) from a counter in the caller's workspace, heaviest rows first.  A unit is two 128-row query tiles that share one stream of
+// rows) from a counter in the caller's workspace, longest units first.  A
+// unit is two 128-row query tiles that share one stream of
 // 128-key KV tiles: the union of the nonzero blocks of both tiles, read from
 // the mask-info block classes (hstu_ops `_next_nonzero`: 0 empty, 1
 // partial, 2 full).  Empty KV tiles are never loaded (splash notes section
 // 21); the element mask is evaluated on partial tiles only.
 //
-// Warp roles (384 threads):
-//   warp 10     takes work units from the counter and builds each unit's
+// Warp roles (384 threads, three warpgroups; the first gives registers to
+// the other two with setmaxnreg):
+//   warp 3      takes work units from the counter and builds each unit's
 //               KV-tile list, up to two units ahead (three list buffers).
 //   warp 0      issues TMA loads: Q per query tile, K and V tiles through a
 //               ring of shared-memory slots (128-byte swizzle).
-//   warps 1,11  one MMA issuer per query tile (warp 1 also allocates the 512
+//   warps 1,2   one MMA issuer per query tile (warp 1 also allocates the 512
 //               TMEM columns): from one lane, tcgen05 MMAs S_t = Q_t K^T (both
 //               operands in shared memory) and O_t += P_t V (P_t read from
 //               TMEM, V from shared memory).
-//   warps 2-5   score warpgroup of query tile 0, warps 6-9 of tile 1: one
+//   warps 4-7   score warpgroup of query tile 0, warps 8-11 of tile 1: one
 //               thread per query row (its TMEM lane).  Softmax: online
 //               max/sum with the correction of the splash notes section 15
 //               (O is rescaled in TMEM only when the running max grew by more
@@ -43,6 +45,12 @@ __device__ int g_fwd_error[4];
 namespace {
 
 constexpr int kThreads = 384;
+// Register split: warpgroup 0 (load, MMA, list) drops to kRegsLight per
+// thread, the two score warpgroups rise to kRegsScore.  Their sum must stay
+// within what the CTA was launched with (kThreads x the kernel's register
+// count), which the launcher checks.
+constexpr uint32_t kRegsLight = 72, kRegsScore = 208;
+constexpr int kRegsNeeded = 128 * kRegsLight + 256 * kRegsScore;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3, kRoleList = 4;
@@ -558,25 +566,42 @@ __device__ __forceinline__ void segment_bits(uint32_t keep[4],
   }
 }
 
-// Masks S of a partial tile in place: columns outside [lo_c, hi_c] or with a
-// cleared keep bit become -inf.
+// Masks S of a partial tile in place: columns outside [lo_c, hi_c] (and,
+// with use_keep, columns whose keep bit is clear) become -inf.  Each thread
+// holds one row.  Per 32-column chunk the row's visible columns are built as
+// one bit word from the two bounds; a chunk that all 32 rows of the warp see
+// whole (a warp-uniform test) is left alone, the others cost one bit test
+// and one select per column.  Under causal and packed-segment masks most
+// chunks of a partial tile are whole for the warp.
 __device__ __forceinline__ void mask_tile(float* s, int lo_c, int hi_c,
-                                          const uint32_t keep[4]) {
+                                          const uint32_t keep[4],
+                                          bool use_keep) {
   const float NEG_INF = __int_as_float(0xff800000);
 #pragma unroll
-  for (int c = 0; c < kTileN; ++c) {
-    const bool vis = (c >= lo_c) && (c <= hi_c) &&
-                     ((keep[c / 32] >> (c % 32)) & 1u);
-    s[c] = vis ? s[c] : NEG_INF;
+  for (int q = 0; q < kTileN / 32; ++q) {
+    const int c0 = 32 * q;
+    // visible columns of this chunk as bits: [lo_c, hi_c] cut to the chunk
+    const int lb = min(max(lo_c - c0, 0), 32), hb = min(max(hi_c - c0 + 1, 0), 32);
+    const uint32_t below_hi = hb >= 32 ? 0xffffffffu : (1u << hb) - 1u;
+    const uint32_t below_lo = lb >= 32 ? 0xffffffffu : (1u << lb) - 1u;
+    uint32_t vm = below_hi & ~below_lo;
+    if (use_keep) vm &= keep[q];
+    if (!__all_sync(0xffffffffu, vm == 0xffffffffu)) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        s[c0 + c] = (vm & (1u << c)) ? s[c0 + c] : NEG_INF;
+    }
   }
 }
 
-template <int D, int SCORE>
+// SEG_ELEM: segment ids are compared element by element (some key-id row is
+// not sorted); otherwise every mask is a key range per row.
+template <int D, int SCORE, bool SEG_ELEM>
 __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
                                            const uint16_t* lists,
                                            uint32_t tmem) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = (warp - 2) / 4;  // query tile of this warpgroup
+  const int t = (warp - 4) / 4;  // query tile of this warpgroup
   const int quarter = warp % 4;  // TMEM lane quarter this warp may access
   const int r = quarter * 32 + lane;
   const bool tracer = (r == 0);
@@ -586,7 +611,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
   volatile int* abort_flag = &bars->abort;
   const float NEG_INF = __int_as_float(0xff800000);
   const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
-  const bool seg_elem = seg && (*p.seg_flags & 1) != 0;
+  constexpr bool seg_elem = SEG_ELEM;
   uint32_t s_cnt = 0, pv_cnt = 0;
   for (int ui = 0;; ++ui) {
     const int buf = ui % kListBufs;
@@ -632,7 +657,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       const int jt = static_cast<int>(ent >> 4);
       const int kbase = jt * kTileN;
       uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (cls == 1 && seg_elem)
+      if (SEG_ELEM && cls == 1)
         segment_bits(keep, segk_b + kbase, min(kTileN, p.Skv - kbase), segq);
       ok = warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, p.timeout_ns);
       if (!ok) {
@@ -648,7 +673,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         tmem_ld32(s_addr + q * 32, sraw + q * 32);
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sraw);
-      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep);
+      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep, seg_elem);
 
       uint32_t pk[16];
       if (SCORE == BSM_SCORE_SOFTMAX) {
@@ -839,14 +864,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    load_role<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, lists);
-  } else if (warp == 10) {
-    list_role(p, bars, lists);
-  } else if (warp == 1 || warp == 11) {
-    mma_role<D>(p, smem, bars, lists, tmem, warp == 1 ? 0 : 1);
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLight>();
+    if (warp == 0)
+      load_role<D>(p, &tm_q, &tm_k, &tm_v, smem, bars, lists);
+    else if (warp == 3)
+      list_role(p, bars, lists);
+    else
+      mma_role<D>(p, smem, bars, lists, tmem, warp - 1);
   } else {
-    score_role<D, SCORE>(p, bars, lists, tmem);
+    setmaxnreg_inc<kRegsScore>();
+    // one path per launch: the element-wise segment compare only when a
+    // key-id row is unsorted (read once; the same for every thread)
+    if ((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0)
+      score_role<D, SCORE, true>(p, bars, lists, tmem);
+    else
+      score_role<D, SCORE, false>(p, bars, lists, tmem);
   }
 
   tc_fence_before();
@@ -868,8 +901,14 @@ cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq,
                        int grid, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = splash_fwd_kernel<D, SCORE>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  // the setmaxnreg split must fit the registers the CTA is launched with,
+  // else the score warps would wait for registers forever
+  if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

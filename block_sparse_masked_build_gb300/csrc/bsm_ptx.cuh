@@ -307,4 +307,15 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b,
                : "memory");
 }
 
+// Warpgroup register reallocation (all 128 threads of the warpgroup run
+// the same instruction).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 }  // namespace bsm
