@@ -677,15 +677,17 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
 
       uint32_t pk[16];
       if (SCORE == BSM_SCORE_SOFTMAX) {
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // row max: three-input max, four independent chains
+        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+        float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 8; c < kTileN; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
         const float m_blk = mx * p.scale_log2;
         bool rescale = false;
         float alpha = 1.f;
@@ -703,14 +705,14 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         for (int q = 0; q < kTileN / 32; ++q) {  // 32 columns at a time
 #pragma unroll
           for (int c = 32 * q; c < 32 * q + 32; c += 4) {
-            const float p0 = ex2_approx(fmaf(s[c], p.scale_log2, neg_m));
-            const float p1 = ex2_approx(fmaf(s[c + 1], p.scale_log2, neg_m));
-            const float p2 = ex2_approx(fmaf(s[c + 2], p.scale_log2, neg_m));
-            const float p3 = ex2_approx(fmaf(s[c + 3], p.scale_log2, neg_m));
-            ls0 += p0;
-            ls1 += p1;
-            ls2 += p2;
-            ls3 += p3;
+            // paired f32 FMA/add: the same roundings as one element at a time
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, s[c], s[c + 1], p.scale_log2, neg_m);
+            ffma2(x2, x3, s[c + 2], s[c + 3], p.scale_log2, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(ls0, ls1, ls0, ls1, p0, p1);
+            fadd2(ls2, ls3, ls2, ls3, p2, p3);
             pk[(c & 31) / 2] = pack_bf16x2(p0, p1);
             pk[(c & 31) / 2 + 1] = pack_bf16x2(p2, p3);
           }
