@@ -401,6 +401,12 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale = scale;
   p.inv_sq = Sq > 0 ? static_cast<float>(1.0 / static_cast<double>(Sq)) : 0.f;
+  // pointwise: x sigmoid(x) / Sq = g (1 + tanh(x / 2)), x = scale s,
+  // g = x / (2 Sq)
+  p.pw_half = static_cast<float>(0.5 * static_cast<double>(scale));
+  p.pw_g = Sq > 0 ? static_cast<float>(0.5 * static_cast<double>(scale) /
+                                        static_cast<double>(Sq))
+                  : 0.f;
   p.out = static_cast<uint16_t*>(out);
   p.o_sb = o_strides[0];
   p.o_sh = o_strides[1];

@@ -741,20 +741,20 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
           }
         }
       } else {
-        // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked (-inf) -> 0
+        // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked (-inf) -> 0.
+        // With sigmoid(x) = (1 + tanh(x/2)) / 2 this is g + g*tanh(x/2),
+        // g = x / (2 Sq): one tanh per element, the rest on paired f32.
 #pragma unroll
         for (int q = 0; q < kTileN / 32; ++q) {
 #pragma unroll
           for (int c = 32 * q; c < 32 * q + 32; c += 2) {
-            float pv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float x = s[c + u] * p.scale;
-              const float sg =
-                  rcp_approx(1.f + ex2_approx(-1.4426950408889634f * x));
-              pv[u] = (s[c + u] != NEG_INF) ? x * sg * p.inv_sq : 0.f;
-            }
-            pk[(c & 31) / 2] = pack_bf16x2(pv[0], pv[1]);
+            float h0, h1, g0, g1, p0, p1;
+            fmul2(h0, h1, s[c], s[c + 1], p.pw_half);
+            fmul2(g0, g1, s[c], s[c + 1], p.pw_g);
+            ffma2v(p0, p1, g0, g1, tanh_approx(h0), tanh_approx(h1), g0, g1);
+            p0 = s[c] != NEG_INF ? p0 : 0.f;
+            p1 = s[c + 1] != NEG_INF ? p1 : 0.f;
+            pk[(c & 31) / 2] = pack_bf16x2(p0, p1);
           }
           tmem_st16(s_addr + q * 16, pk);
         }

@@ -64,6 +64,8 @@ struct FwdParams {
   float scale_log2;  // softmax: scale * log2(e)
   float scale;       // pointwise
   float inv_sq;      // pointwise: 1 / Sq
+  float pw_half;     // pointwise: scale / 2
+  float pw_g;        // pointwise: scale / (2 Sq)
   // outputs
   uint16_t* out;  // bf16 bits
   int64_t o_sb, o_sh, o_ss;
