@@ -411,6 +411,11 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.o_sb = o_strides[0];
   p.o_sh = o_strides[1];
   p.o_ss = o_strides[2];
+  p.o_vec8 = (reinterpret_cast<uintptr_t>(out) % 32 == 0 &&
+              o_strides[0] % 16 == 0 && o_strides[1] % 16 == 0 &&
+              o_strides[2] % 16 == 0)
+                 ? 1
+                 : 0;
   p.lse = lse;
   p.unit_counter = static_cast<int32_t*>(workspace);
   p.lists = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + 256);

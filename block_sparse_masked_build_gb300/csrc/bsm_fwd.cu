@@ -108,8 +108,8 @@ struct TraceRec {
 enum : uint32_t {
   kEvListBuilt = 1, kEvQIssued = 2, kEvMmaUnit = 3, kEvMmaLastPv = 4,
   kEvSFull = 5, kEvPFull = 6, kEvEpiBegin = 7, kEvEpiEnd = 8, kEvRescale = 9,
-  kEvKReady = 10, kEvSIssued = 11, kEvPReady = 12, kEvPVIssued = 13,
-  kEvVReady = 14, kEvTmaIssued = 15
+  kEvEpiPvLanded = 10, kEvSIssued = 11, kEvPReady = 12, kEvPVIssued = 13,
+  kEvEpiOLoaded = 14, kEvTmaIssued = 15
 };
 
 __device__ __forceinline__ void trace(const FwdParams& p, Bars* bars,
@@ -779,29 +779,46 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         record_timeout(kRoleScore, 3);
         break;
       }
+      if (tracer) trace(p, bars, kRoleScore, kEvEpiPvLanded, t, 0, unit);
       tc_fence_after();
+      // all of O_t into registers with one wait; the next unit's first P.V
+      // may then overwrite it while the stores go out
+      uint32_t o[D];
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) tmem_ld32(o_addr + q * 32, o + q * 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      if (tracer) trace(p, bars, kRoleScore, kEvEpiOLoaded, t, 0, unit);
       float inv = 1.f;
       if (SCORE == BSM_SCORE_SOFTMAX) inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-#pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + q * 32, o);
-        tmem_ld_wait();
-        uint32_t w[16];
+      if (row_ok) {
+        // 32 bytes per store where the row alignment allows: each warp
+        // store touches 32 rows, so fewer, wider stores cost fewer requests
+        const bool v8 = p.o_vec8 != 0;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv,
-                             __uint_as_float(o[2 * c + 1]) * inv);
-        if (row_ok) {
+        for (int v = 0; v < D / 16; ++v) {
+          uint32_t w[8];
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            st_global_v4(orow + q * 32 + v * 8, w[4 * v], w[4 * v + 1],
-                         w[4 * v + 2], w[4 * v + 3]);
+          for (int c = 0; c < 8; ++c)
+            w[c] = pack_bf16x2(__uint_as_float(o[16 * v + 2 * c]) * inv,
+                               __uint_as_float(o[16 * v + 2 * c + 1]) * inv);
+          if (v8) {
+            st_global_v8(orow + v * 16, w);
+          } else {
+            st_global_v4(orow + v * 16, w[0], w[1], w[2], w[3]);
+            st_global_v4(orow + v * 16 + 8, w[4], w[5], w[6], w[7]);
+          }
         }
       }
-    } else if (row_ok) {
+    } else {
+      if (row_ok) {
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v) st_global_v4(orow + v * 8, 0u, 0u, 0u, 0u);
+        for (int v = 0; v < D / 8; ++v)
+          st_global_v4(orow + v * 8, 0u, 0u, 0u, 0u);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
     }
     if (SCORE == BSM_SCORE_SOFTMAX && p.lse != nullptr && row_ok) {
       const float lse = l_sum > 0.f
@@ -809,8 +826,6 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
                             : NEG_INF;
       p.lse[(static_cast<int64_t>(uc.b) * p.H + uc.h) * p.Sq + qrow] = lse;
     }
-    tc_fence_before();
-    mbar_arrive(&bars->o_free[t]);
     mbar_arrive(&bars->list_free[buf]);
     if (tracer) trace(p, bars, kRoleScore, kEvEpiEnd, t, 0, unit);
   }

@@ -69,6 +69,7 @@ struct FwdParams {
   // outputs
   uint16_t* out;  // bf16 bits
   int64_t o_sb, o_sh, o_ss;
+  int32_t o_vec8;  // out and its strides allow 32-byte row stores
   float* lse;
   int32_t* unit_counter;  // workspace: next work unit (zeroed per launch)
   uint16_t* lists;        // workspace: [grid][kListBufs][kMaxKvTiles]

@@ -338,6 +338,15 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1,
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// 32-byte store of eight words; `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t w[8]) {
+  asm volatile(
+      "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+      "r"(w[6]), "r"(w[7])
+      : "memory");
+}
+
 // Warpgroup register reallocation (all 128 threads of the warpgroup run
 // the same instruction).
 template <uint32_t N>

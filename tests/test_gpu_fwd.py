@@ -156,6 +156,25 @@ def test_unit_order_does_not_change_results(flags):
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_padded_output_rows_match(D):
+    # an output row stride of D + 8 elements (16-byte but not 32-byte
+    # aligned rows) takes the narrower store path; results are identical
+    B, H, S = 1, 2, 384
+    q, k, v = _qkv(B, H, H, S, S, D, seed=15)
+    a, la, info = run_gpu(q, k, v, C, 0, None, None, 0.1, SM)
+    dev = torch.device("cuda")
+    big = torch.full((B, H, S, D + 8), float("nan"), dtype=torch.bfloat16,
+                     device=dev)
+    out = big[..., :D]
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    bsm.bsm_splash_fwd(q.to(dev), k.to(dev), v.to(dev), info, None, None, 0.1,
+                       SM, out, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out.float().cpu(), a) and torch.equal(lse.cpu(), la)
+    assert torch.isnan(big[..., D:].float()).all()
+
+
 def test_repeated_calls_are_deterministic():
     B, H, S, D = 2, 4, 1024, 128
     q, k, v = _qkv(B, H, H, S, S, D, seed=12)
