@@ -52,6 +52,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kRegsLight = 72, kRegsScore = 208;
 constexpr int kRegsNeeded = 128 * kRegsLight + 256 * kRegsScore;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kPingPongMin = 12;  // see score_role
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3, kRoleList = 4;
 
@@ -59,7 +60,7 @@ template <int D>
 struct Cfg {
   static constexpr int kKBlocks = D / 64;            // 128-byte k-blocks
   static constexpr int kTileBytes = kTileM * D * 2;  // Q, K or V tile
-  static constexpr int kSlots = (D == 128) ? 5 : 8;
+  static constexpr int kSlots = (D == 128) ? 3 : 8;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
@@ -80,6 +81,8 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[8], kv_empty[8];  // up to 8 ring slots
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
+  // softmax turn of each score warp: [query tile][TMEM lane quarter]
+  uint64_t sm_turn[2][4];
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
@@ -596,7 +599,7 @@ __device__ __forceinline__ void mask_tile(float* s, int lo_c, int hi_c,
 
 // SEG_ELEM: segment ids are compared element by element (some key-id row is
 // not sorted); otherwise every mask is a key range per row.
-template <int D, int SCORE, bool SEG_ELEM>
+template <int D, int SCORE, bool SEG_ELEM, bool PINGPONG>
 __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
                                            const uint16_t* lists,
                                            uint32_t tmem) {
@@ -612,7 +615,11 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
   const float NEG_INF = __int_as_float(0xff800000);
   const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
   constexpr bool seg_elem = SEG_ELEM;
-  uint32_t s_cnt = 0, pv_cnt = 0;
+  uint32_t s_cnt = 0, pv_cnt = 0, turns = 0;
+  auto pass_turn = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->sm_turn[1 - t][quarter]);
+  };
   for (int ui = 0;; ++ui) {
     const int buf = ui % kListBufs;
     if (!warp_wait(&bars->list_full[buf], (ui / kListBufs) & 1, abort_flag,
@@ -654,6 +661,25 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       const int cls = t == 0 ? static_cast<int>((ent >> 2) & 3u)
                              : static_cast<int>(ent & 3u);
       if (!cls) continue;
+      // On entries both tiles use, softmax turns alternate between the two
+      // score warps that share an SM sub-partition (same lane quarter,
+      // tiles 0 and 1; tile 0 first): one works while the tensor core runs
+      // the other tile's P.V and next S, instead of both competing for the
+      // same issue slots and MUFU at once.
+      // (only in units of at least kPingPongMin entries: in a short unit
+      // the two tiles would spend a softmax setting up the alternation)
+      const bool shared = PINGPONG && n_ent >= kPingPongMin &&
+                          ((ent >> 2) & 3u) != 0 && (ent & 3u) != 0;
+      if (shared) {
+        ok = warp_wait(&bars->sm_turn[t][quarter],
+                       (turns & 1) ^ (t == 0 ? 1u : 0u), abort_flag,
+                       p.timeout_ns);
+        if (!ok) {
+          record_timeout(kRoleScore, 6);
+          break;
+        }
+        ++turns;
+      }
       const int jt = static_cast<int>(ent >> 4);
       const int kbase = jt * kTileN;
       uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
@@ -762,6 +788,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
+      if (shared) pass_turn();
       if (tracer) trace(p, bars, kRoleScore, kEvPFull, t, e, unit);
       ++pv_cnt;
       ++unit_pv;
@@ -831,7 +858,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
   }
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, bool PINGPONG>
 __global__ void __launch_bounds__(kThreads, 1)
     splash_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -858,6 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[i], kTileM);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->o_free[i], kTileM);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->sm_turn[i][q], 1);
     }
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&bars->kv_full[i], 1);
@@ -894,9 +922,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one path per launch: the element-wise segment compare only when a
     // key-id row is unsorted (read once; the same for every thread)
     if ((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0)
-      score_role<D, SCORE, true>(p, bars, lists, tmem);
+      score_role<D, SCORE, true, PINGPONG>(p, bars, lists, tmem);
     else
-      score_role<D, SCORE, false>(p, bars, lists, tmem);
+      score_role<D, SCORE, false, PINGPONG>(p, bars, lists, tmem);
   }
 
   tc_fence_before();
@@ -912,12 +940,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int SCORE>
+template <int D, int SCORE, bool PINGPONG>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv,
                        int grid, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = splash_fwd_kernel<D, SCORE>;
+  auto kern = splash_fwd_kernel<D, SCORE, PINGPONG>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
@@ -958,12 +986,25 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               int num_sms, cudaStream_t stream) {
   const int grid = fwd_grid_size(p, num_sms);
   const bool pw = p.score == BSM_SCORE_POINTWISE;
-  if (p.D == 128)
-    return pw ? launch_one<128, BSM_SCORE_POINTWISE>(p, tq, tk, tv, grid, stream)
-              : launch_one<128, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, grid, stream);
-  if (p.D == 64)
-    return pw ? launch_one<64, BSM_SCORE_POINTWISE>(p, tq, tk, tv, grid, stream)
-              : launch_one<64, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, grid, stream);
+  // Softmax turns alternate between the tiles only where work units are
+  // long: no segment ids and at least 4096 keys.  Packed sequences and
+  // short sequences give short units, where the alternation costs more
+  // than it saves.
+  const bool pp = (p.flags & BSM_MASK_SEGMENT) == 0 && p.Skv >= 4096;
+  if (p.D == 128) {
+    if (pw)
+      return pp ? launch_one<128, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)
+                : launch_one<128, BSM_SCORE_POINTWISE, false>(p, tq, tk, tv, grid, stream);
+    return pp ? launch_one<128, BSM_SCORE_SOFTMAX, true>(p, tq, tk, tv, grid, stream)
+              : launch_one<128, BSM_SCORE_SOFTMAX, false>(p, tq, tk, tv, grid, stream);
+  }
+  if (p.D == 64) {
+    if (pw)
+      return pp ? launch_one<64, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)
+                : launch_one<64, BSM_SCORE_POINTWISE, false>(p, tq, tk, tv, grid, stream);
+    return pp ? launch_one<64, BSM_SCORE_SOFTMAX, true>(p, tq, tk, tv, grid, stream)
+              : launch_one<64, BSM_SCORE_SOFTMAX, false>(p, tq, tk, tv, grid, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -68,6 +68,12 @@ SMALL = [
     ("gqa", 1, 4, 2, 512, 512, 128, C, 0, SM, 128, 128),
     ("blocks_256", 1, 2, 2, 768, 768, 128, C, 0, SM, 256, 256),
     ("blocks_mixed", 1, 2, 2, 640, 640, 128, C, 0, SM, 64, 256),
+    # at least 4096 keys without segments: the kernel whose score warps
+    # alternate softmax turns between the two query tiles
+    ("long_causal_pingpong", 1, 1, 1, 4096, 4096, 128, C, 0, SM, 128, 128),
+    ("long_local_pingpong", 1, 1, 1, 4500, 4500, 128, C | L, 1500, SM, 128,
+     128),
+    ("long_pointwise_pingpong", 1, 1, 1, 4096, 4096, 128, C, 0, PW, 128, 128),
 ]
 
 
