@@ -281,6 +281,10 @@ def run_ours(args, w, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
 
+    info0 = bsm.bsm_build_mask_info(w.flags, w.window, segd, segd, w.B, w.Sq,
+                                    w.Skv_, w.block_q, w.block_kv, mibuf,
+                                    stream)
+    mi_bytes = mask_info_bytes(w, info0)
     K = args.steps
     if K is None:  # about 1.5 s of timed work so the clock samples mean something
         e0 = torch.cuda.Event(enable_timing=True)
@@ -348,8 +352,8 @@ def run_ours(args, w, world, rank, local):
             "traffic": traffic,
             "algorithmic_bytes": algorithmic_bytes(w),
             "fwd_ms": round(fwd_mean, 5)},
-        "mask_info": {"ms": round(statistics.fmean(mi_ms), 5),
-                      "launches": 3 + (1 if w.flags & wl.MASK_SEGMENT else 0)},
+        "mask_info": mask_info_line(w, mi_bytes, statistics.fmean(mi_ms),
+                                    peaks),
         "gpu_launches": (LAUNCHES_PER_STEP
                          + (1 if w.flags & wl.MASK_SEGMENT else 0)) * K,
         "clocks": clocks,
@@ -358,6 +362,32 @@ def run_ours(args, w, world, rank, local):
     if e2e is not None:
         line["e2e"] = e2e
     return line
+
+
+def mask_info_bytes(w, info):
+    """Algorithmic HBM bytes of one mask-info build: segment ids read once,
+    every table written once (block classes, next-block table, CSR offsets,
+    the nonzero lists, segment ranges, longest-first order)."""
+    s = info.struct
+    T, nq, nk = s.num_tables, s.nq, s.nk
+    cells = T * nq * nk
+    nnz = int(info.row_ptr[-1].item())
+    seg = bool(w.flags & wl.MASK_SEGMENT)
+    read = 4 * w.B * (w.Sq + w.Skv_) if seg else 0
+    written = (cells + 4 * cells + 4 * (T * nq + 1) + 5 * nnz
+               + (8 * w.B * w.Sq + 4 if seg else 0)
+               + (4 * T * s.num_super if s.super_order else 0))
+    return read + written
+
+
+def mask_info_line(w, nbytes, ms, peaks):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5),
+            "launches": 3 + (1 if w.flags & wl.MASK_SEGMENT else 0),
+            "bound": "launch latency (a few small kernels)",
+            "algorithmic_bytes": nbytes, "achieved": round(gbs, 2),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 5)}
 
 
 def algorithmic_bytes(w):
