@@ -354,8 +354,7 @@ def run_ours(args, w, world, rank, local):
             "fwd_ms": round(fwd_mean, 5)},
         "mask_info": mask_info_line(w, mi_bytes, statistics.fmean(mi_ms),
                                     peaks),
-        "gpu_launches": (LAUNCHES_PER_STEP
-                         + (1 if w.flags & wl.MASK_SEGMENT else 0)) * K,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks,
         "wall_s_timed": round(t_wall1 - t_wall0, 3),
     }
@@ -383,7 +382,7 @@ def mask_info_bytes(w, info):
 def mask_info_line(w, nbytes, ms, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"ms": round(ms, 5),
-            "launches": 3 + (1 if w.flags & wl.MASK_SEGMENT else 0),
+            "launches": 3,
             "bound": "launch latency (a few small kernels)",
             "algorithmic_bytes": nbytes, "achieved": round(gbs, 2),
             "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -60,8 +60,8 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows,
   o = align_up(o + cells, 256);
   L.off_sr = o;
   o = align_up(o + static_cast<size_t>(seg_rows) * 8, 256);
-  L.off_sf = o;
-  o = align_up(o + 4, 256);
+  L.off_sf = o;  // [0]: any table unsorted; [1 + t]: table t (builder scratch)
+  o = align_up(o + 4 * (1 + (seg_rows > 0 ? tables : 0)), 256);
   L.off_so = o;
   if (pairs <= bsm::kMaxSuperOrder)
     o = align_up(o + static_cast<size_t>(pairs) * 4, 256);

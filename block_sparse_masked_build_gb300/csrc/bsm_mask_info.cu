@@ -6,18 +6,20 @@
 // next nonzero block) plus per-row CSR lists of the nonzero blocks.
 //
 // Launches:
-//   0. (segment ids only) segment ranges: for every query row, the first and
-//      last key whose id equals the row's (binary search; exact when each kv
-//      id row is non-decreasing, as for packed sequences), and a flag set if
-//      some kv id row is not sorted.
 //   1. classify: one CTA per (table, q-block row).  Causal/local blocks are
 //      classified exactly from the range of q - k over the block.  With
-//      segment ids and sorted kv ids, every row's visible keys form one
+//      segment ids the CTA first stages the table's kv ids in shared memory
+//      (up to kStagedKeys of them), checks that they are non-decreasing, and
+//      finds for each of its query rows the first and last key with the
+//      row's id (binary search; exact for sorted ids, as for packed
+//      sequences).  With sorted ids every row's visible keys form one
 //      interval, so a block is classified from its rows' intervals; with
 //      unsorted ids the min/max of the ids settle most blocks and the rest
-//      are scanned element by element.  Writes block_mask, data_next and the
-//      row's nonzero count.
-//   2. scan: one CTA turns the counts into CSR row offsets.
+//      are scanned element by element.  Writes block_mask, data_next, the
+//      row's nonzero count, the rows' segment ranges and the table's
+//      "not sorted" bit.
+//   2. scan: one CTA turns the counts into CSR row offsets, ORs the tables'
+//      "not sorted" bits into seg_flags[0] and orders the super-tiles.
 //   3. compact: one CTA per row writes the ascending nonzero list.
 #include <cstdint>
 
@@ -27,6 +29,21 @@ namespace bsm {
 namespace {
 
 constexpr int kMiThreads = 256;
+constexpr int kStagedKeys = 32768;  // kv ids staged in shared memory (128 KB)
+
+__host__ __device__ constexpr int cls_bytes(int nk) { return (nk + 15) & ~15; }
+
+// First index in ks[0, n) whose id is >= v (or > v with `after`).
+__device__ __forceinline__ int id_search(const int32_t* ks, int n, int v,
+                                         bool after) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int x = ks[mid];
+    if (x < v || (after && x == v)) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
 constexpr int kNegInf = -(1 << 30);
 constexpr int kPosInf = (1 << 30);
 
@@ -65,40 +82,12 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
   return v;
 }
 
-// Per query row: [first, last] key index with the row's segment id (binary
-// search in the sorted kv ids), and the "kv ids not sorted" flag.
-__global__ void __launch_bounds__(kMiThreads)
-    mi_segrange_kernel(const MaskInfoParams p) {
-  const int t = blockIdx.y;
-  const int32_t* qs = p.q_seg + static_cast<int64_t>(t) * p.Sq;
-  const int32_t* ks = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k + 1 < p.Skv;
-       k += gridDim.x * blockDim.x) {
-    if (ks[k] > ks[k + 1]) atomicOr(p.seg_flags, 1);
-  }
-  const int q = blockIdx.x * blockDim.x + threadIdx.x;
-  if (q >= p.Sq) return;
-  const int v = qs[q];
-  int lo = 0, hi = p.Skv;  // first index with ks >= v
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (ks[mid] < v) lo = mid + 1; else hi = mid;
-  }
-  int lo2 = lo, hi2 = p.Skv;  // first index with ks > v
-  while (lo2 < hi2) {
-    const int mid = (lo2 + hi2) >> 1;
-    if (ks[mid] <= v) lo2 = mid + 1; else hi2 = mid;
-  }
-  int2 r;
-  r.x = lo;
-  r.y = lo2 - 1;
-  reinterpret_cast<int2*>(p.seg_range)[static_cast<int64_t>(t) * p.Sq + q] = r;
-}
-
 __global__ void __launch_bounds__(kMiThreads)
     mi_classify_kernel(const MaskInfoParams p) {
-  extern __shared__ int8_t cls_s[];  // [nk]
+  extern __shared__ __align__(16) uint8_t dyn_s[];
+  int8_t* cls_s = reinterpret_cast<int8_t*>(dyn_s);  // [nk]
   __shared__ int qseg_s[512];
+  __shared__ int2 sr_s[512];
   __shared__ int red_min[kMiThreads / 32], red_max[kMiThreads / 32];
   __shared__ int cnt_s;
 
@@ -136,10 +125,37 @@ __global__ void __launch_bounds__(kMiThreads)
     }
   }
 
-  const bool ranges = seg && (*p.seg_flags & 1) == 0;
-  const int2* sr = ranges ? reinterpret_cast<const int2*>(p.seg_range) +
-                                static_cast<int64_t>(t) * p.Sq
-                          : nullptr;
+  // kv ids of this table: staged in shared memory when they fit
+  const int32_t* ks = nullptr;
+  bool sorted = true;
+  if (seg) {
+    const int32_t* ks_g = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
+    ks = ks_g;
+    if (p.Skv <= kStagedKeys) {
+      int32_t* ks_s = reinterpret_cast<int32_t*>(dyn_s + cls_bytes(p.nk));
+      for (int k = threadIdx.x; k < p.Skv; k += blockDim.x) ks_s[k] = ks_g[k];
+      __syncthreads();
+      ks = ks_s;
+    }
+    bool unsorted = false;
+    for (int k = threadIdx.x; k + 1 < p.Skv; k += blockDim.x)
+      unsorted |= ks[k] > ks[k + 1];
+    sorted = !__syncthreads_or(unsorted);
+    if (i == 0 && threadIdx.x == 0) p.seg_flags[1 + t] = sorted ? 0 : 1;
+    // each row's [first, last] key with its id (first > last: none)
+    int2* sr_g = reinterpret_cast<int2*>(p.seg_range) +
+                 static_cast<int64_t>(t) * p.Sq;
+    for (int r = r0 + threadIdx.x; r <= r1; r += blockDim.x) {
+      const int v = qseg_s[r - r0];
+      int2 rg;
+      rg.x = id_search(ks, p.Skv, v, false);
+      rg.y = id_search(ks, p.Skv, v, true) - 1;
+      sr_s[r - r0] = rg;
+      sr_g[r] = rg;
+    }
+    __syncthreads();
+  }
+  const bool ranges = seg && sorted;
 
   // One warp per block (i, j).
   int my_count = 0;
@@ -150,7 +166,8 @@ __global__ void __launch_bounds__(kMiThreads)
       // each row sees one interval of keys: count it inside the block
       bool any = false, all = !br.ragged;
       for (int q = br.r0 + lane; q <= br.r1; q += 32) {
-        int lo = max(br.c0, sr[q].x), hi = min(br.c1, sr[q].y);
+        int lo = max(br.c0, sr_s[q - br.r0].x),
+            hi = min(br.c1, sr_s[q - br.r0].y);
         if (p.flags & BSM_MASK_CAUSAL) hi = min(hi, q);
         if (p.flags & BSM_MASK_LOCAL) lo = max(lo, q - p.window + 1);
         const int n = hi >= lo ? hi - lo + 1 : 0;
@@ -161,7 +178,6 @@ __global__ void __launch_bounds__(kMiThreads)
       all = __all_sync(0xffffffffu, all);
       c = any ? (all ? 2 : 1) : 0;
     } else if (seg && c != 0) {
-      const int32_t* ks = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
       int kmin = kPosInf, kmax = kNegInf;
       for (int k = br.c0 + lane; k <= br.c1; k += 32) {
         const int v = ks[k];
@@ -278,6 +294,13 @@ __global__ void __launch_bounds__(1024) mi_scan_kernel(const MaskInfoParams p) {
     if (threadIdx.x == blockDim.x - 1) carry_s = carry + warp_sums[31];
     __syncthreads();
   }
+  if (p.flags & BSM_MASK_SEGMENT) {  // any table's kv ids not sorted
+    int any = 0;
+    for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
+      any |= p.seg_flags[1 + tb];
+    any = __syncthreads_or(any);
+    if (threadIdx.x == 0) p.seg_flags[0] = any ? 1 : 0;
+  }
   if (p.super_order == nullptr) return;
 
   // ---- longest-first order of the (table, super-tile) pairs
@@ -371,15 +394,15 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
     return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t), stream);
   }
   cudaError_t e;
-  if (p.flags & BSM_MASK_SEGMENT) {
-    e = cudaMemsetAsync(p.seg_flags, 0, sizeof(int32_t), stream);
-    if (e != cudaSuccess) return e;
-    const int gx = (max(p.Sq, 1) + kMiThreads - 1) / kMiThreads;
-    mi_segrange_kernel<<<dim3(gx, p.tables), kMiThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
+  size_t smem = static_cast<size_t>(cls_bytes(p.nk > 0 ? p.nk : 1));
+  if ((p.flags & BSM_MASK_SEGMENT) && p.Skv <= kStagedKeys)
+    smem += static_cast<size_t>(p.Skv) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(mi_classify_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  const size_t smem = static_cast<size_t>(p.nk > 0 ? p.nk : 1);
   mi_classify_kernel<<<dim3(p.nq, p.tables), kMiThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -81,7 +81,8 @@ typedef struct bsm_mask_spec {
  *                       when no key has q's id
  *   seg_flags[0]        int32 (SEGMENT only): bit 0 set if some kv segment-id
  *                       row is not non-decreasing (then seg_range is unused and
- *                       segments are compared element by element)
+ *                       segments are compared element by element); entries
+ *                       1..num_tables are the builder's per-table scratch
  *   super_order[k]      int32, num_tables*num_super entries: the pairs
  *                       (table t, super-tile s) as t*num_super + s, ordered by
  *                       decreasing work (query rows times nonzero blocks

@@ -66,7 +66,8 @@ def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
     pairs = T * -(-Sq // 256)  # (table, 256-row super-tile) pairs
     want = (_align(cells) + _align(4 * cells) + _align(4 * (T * nq + 1))
             + _align(4 * cells) + _align(cells) + _align(8 * seg_rows)
-            + _align(4) + (_align(4 * pairs) if pairs <= 8192 else 0))
+            + _align(4 * (1 + (T if flags & 4 else 0)))
+            + (_align(4 * pairs) if pairs <= 8192 else 0))
     spec = MaskSpec(flags, 4096 if flags & 2 else 0)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv, bq,
                                    bkv) == want
