@@ -19,8 +19,10 @@
 //      row's nonzero count, the rows' segment ranges and the table's
 //      "not sorted" bit.
 //   2. scan: one CTA turns the counts into CSR row offsets, ORs the tables'
-//      "not sorted" bits into seg_flags[0] and orders the super-tiles.
-//   3. compact: one CTA per row writes the ascending nonzero list.
+//      "not sorted" bits into seg_flags[0] and orders the super-tiles; for
+//      masks of up to 2^14 block cells it also writes the nonzero lists.
+//   3. compact (larger masks only): one CTA per row writes the ascending
+//      nonzero list.
 #include <cstdint>
 
 #include "bsm_internal.h"
@@ -30,6 +32,27 @@ namespace {
 
 constexpr int kMiThreads = 256;
 constexpr int kStagedKeys = 32768;  // kv ids staged in shared memory (128 KB)
+// Masks of at most this many block cells are compacted by the scan kernel
+// itself (one launch fewer); larger ones by one CTA per row.
+constexpr int64_t kFusedCompactCells = int64_t{1} << 14;
+
+// Ascending list of the nonzero blocks of row `row`, written by one warp.
+__device__ __forceinline__ void compact_row_warp(const MaskInfoParams& p,
+                                                 int64_t row, int lane) {
+  const int8_t* bm = p.block_mask + row * p.nk;
+  int base = p.row_ptr[row];
+  for (int j0 = 0; j0 < p.nk; j0 += 32) {
+    const int j = j0 + lane;
+    const int8_t c = j < p.nk ? bm[j] : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+    if (c != 0) {
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      p.kv_idx[pos] = j;
+      p.kv_cls[pos] = c;
+    }
+    base += __popc(m);
+  }
+}
 
 __host__ __device__ constexpr int cls_bytes(int nk) { return (nk + 15) & ~15; }
 
@@ -294,6 +317,12 @@ __global__ void __launch_bounds__(1024) mi_scan_kernel(const MaskInfoParams p) {
     if (threadIdx.x == blockDim.x - 1) carry_s = carry + warp_sums[31];
     __syncthreads();
   }
+  if (static_cast<int64_t>(R) * p.nk <= kFusedCompactCells) {
+    __syncthreads();  // row_ptr complete
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    for (int row = warp; row < R; row += blockDim.x / 32)
+      compact_row_warp(p, row, lane);
+  }
   if (p.flags & BSM_MASK_SEGMENT) {  // any table's kv ids not sorted
     int any = 0;
     for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
@@ -409,7 +438,8 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   mi_scan_kernel<<<1, 1024, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);
+  if (static_cast<int64_t>(R) * p.nk > kFusedCompactCells)
+    mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -116,6 +116,26 @@ def test_super_order_absent_above_limit():
     assert got["super_order"] is None and got["num_super"] == 1024
 
 
+def test_large_causal_mask_lists_closed_form():
+    # 1024 x 1024 block cells (more than 2^14: the lists are written by the
+    # separate per-row compaction): causal classes are 2 below the diagonal,
+    # 1 on it, 0 above; each row's list is its nonzero blocks in order
+    S, b = 65536, 64
+    got = _gpu_info(1, 0, None, None, 1, S, S, b, b)
+    n = S // b
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    want = np.where(j < i, 2, np.where(j == i, 1, 0)).astype(np.int8)
+    np.testing.assert_array_equal(got["block_mask"].reshape(n, n), want)
+    rp = got["row_ptr"]
+    np.testing.assert_array_equal(np.diff(rp), np.arange(1, n + 1))
+    for r in (0, 1, 517, n - 1):
+        np.testing.assert_array_equal(got["kv_idx"][rp[r]:rp[r + 1]],
+                                      np.arange(r + 1))
+        np.testing.assert_array_equal(got["kv_cls"][rp[r]:rp[r + 1]],
+                                      np.r_[np.full(r, 2), 1].astype(np.int8))
+
+
 def test_empty_kv_mask_info():
     got = _gpu_info(0, 0, None, None, 1, 100, 0, 64, 64)
     assert got["block_mask"].shape == (1, 2, 0)
