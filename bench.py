@@ -286,6 +286,7 @@ def run_ours(args, w, world, rank, local):
                                     stream)
     mi_bytes = mask_info_bytes(w, info0)
     mi_launches = mask_info_launches(info0)
+    executed_flops = executed_mma_flops(w, info0)
     K = args.steps
     if K is None:  # about 1.5 s of timed work so the clock samples mean something
         e0 = torch.cuda.Event(enable_timing=True)
@@ -327,6 +328,8 @@ def run_ours(args, w, world, rank, local):
     peaks = load_peaks()
     achieved = flops / (fwd_mean * 1e-3) / 1e12
     traffic = recorded_traffic(w.name)
+    roof = forward_roofline(w, flops, fwd_mean, peaks, traffic)
+    roof["executed_mma_flops"] = executed_flops
 
     e2e = None
     if not args.no_e2e:
@@ -344,15 +347,7 @@ def run_ours(args, w, world, rank, local):
                                     if world > 1 else "single GPU")),
         "pct_of_bf16_peak": round(100.0 * value / world / peaks["bf16_tflops"],
                                   2),
-        "roofline": {
-            "kernel": "splash_fwd_kernel", "bound": "tensor",
-            "achieved": round(achieved, 2),
-            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(achieved / peaks["bf16_tflops"], 4),
-            "peak_source": f"{peaks['source']} (burst bf16 GEMM)",
-            "traffic": traffic,
-            "algorithmic_bytes": algorithmic_bytes(w),
-            "fwd_ms": round(fwd_mean, 5)},
+        "roofline": roof,
         "mask_info": mask_info_line(w, mi_bytes, statistics.fmean(mi_ms),
                                     peaks, mi_launches),
         "gpu_launches": (1 + mi_launches) * K,
@@ -395,6 +390,40 @@ def mask_info_line(w, nbytes, ms, peaks, launches):
             "algorithmic_bytes": nbytes, "achieved": round(gbs, 2),
             "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 5)}
+
+
+def executed_mma_flops(w, info):
+    """Block-level MMA work of one forward: nonempty mask blocks x
+    block_q x block_kv x 4 D, over every (batch, head) the tables cover."""
+    s = info.struct
+    nnz = int(info.row_ptr[-1].item())
+    per_table = w.H if s.num_tables > 1 else w.B * w.H
+    return nnz * w.block_q * w.block_kv * 4 * w.D * per_table
+
+
+def forward_roofline(w, flops, fwd_ms, peaks, traffic):
+    """Roofline of the forward kernel: tensor-bound when the unmasked
+    FLOPs per algorithmic byte reach the measured ridge (peak FLOP/s over
+    peak HBM B/s), else HBM-bound and reported in GB/s."""
+    nbytes = algorithmic_bytes(w)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    common = {"kernel": "splash_fwd_kernel", "traffic": traffic,
+              "algorithmic_bytes": nbytes,
+              "flop_per_byte": round(flops / nbytes, 1),
+              "ridge_flop_per_byte": round(ridge, 1),
+              "fwd_ms": round(fwd_ms, 5)}
+    if flops / nbytes >= ridge:
+        achieved = flops / (fwd_ms * 1e-3) / 1e12
+        return dict(common, bound="tensor", achieved=round(achieved, 2),
+                    peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=round(achieved / peaks["bf16_tflops"], 4),
+                    peak_source=f"{peaks['source']} (burst bf16 GEMM)")
+    gbs = nbytes / (fwd_ms * 1e-3) / 1e9
+    return dict(common, bound="hbm", achieved=round(gbs, 2),
+                peak=peaks["hbm_gbs"], unit="GB/s",
+                frac=round(gbs / peaks["hbm_gbs"], 5),
+                peak_source=f"{peaks['source']} (STREAM-style copy)",
+                tflops=round(flops / (fwd_ms * 1e-3) / 1e12, 3))
 
 
 def algorithmic_bytes(w):
