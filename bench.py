@@ -218,7 +218,8 @@ def mask_name(flags, window):
     if flags & wl.MASK_CAUSAL:
         parts.append("causal")
     if flags & wl.MASK_LOCAL:
-        parts.append(f"q-k<{window}")
+        parts.append(f"|q-k|<{window}" if flags & wl.MASK_BAND
+                     else f"q-k<{window}")
     if flags & wl.MASK_SEGMENT:
         parts.append("same-segment")
     return "&".join(parts) or "full"

@@ -20,6 +20,7 @@ from ._lib import MaskInfoStruct, MaskSpec, I64x3
 MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
+MASK_BAND = 8  # with MASK_LOCAL: |q - k| < window
 SCORE_SOFTMAX = 0
 SCORE_POINTWISE = 1
 

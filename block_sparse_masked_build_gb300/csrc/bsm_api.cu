@@ -71,9 +71,12 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows,
 
 bsm_status check_spec(const bsm_mask_spec* spec) {
   if (spec == nullptr) return fail(BSM_ERR_INVALID_ARG, "mask spec is NULL");
-  const uint32_t known = BSM_MASK_CAUSAL | BSM_MASK_LOCAL | BSM_MASK_SEGMENT;
+  const uint32_t known =
+      BSM_MASK_CAUSAL | BSM_MASK_LOCAL | BSM_MASK_SEGMENT | BSM_MASK_BAND;
   if (spec->flags & ~known)
     return fail(BSM_ERR_INVALID_ARG, "unknown mask flag bits");
+  if ((spec->flags & BSM_MASK_BAND) && !(spec->flags & BSM_MASK_LOCAL))
+    return fail(BSM_ERR_INVALID_ARG, "BSM_MASK_BAND needs BSM_MASK_LOCAL");
   if ((spec->flags & BSM_MASK_LOCAL) && spec->window < 1)
     return fail(BSM_ERR_INVALID_ARG, "local window must be >= 1");
   return BSM_OK;

@@ -640,6 +640,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
     int rlo = 0, rhi = p.Skv - 1;
     if (p.flags & BSM_MASK_CAUSAL) rhi = min(rhi, qrow);
     if (p.flags & BSM_MASK_LOCAL) rlo = max(rlo, qrow - p.window + 1);
+    if (p.flags & BSM_MASK_BAND) rhi = min(rhi, qrow + p.window - 1);
     int segq = 0;
     if (seg && row_ok) {
       const int64_t qi = static_cast<int64_t>(uc.b) * p.Sq + qrow;

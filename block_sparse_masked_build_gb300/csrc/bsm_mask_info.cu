@@ -90,7 +90,9 @@ __device__ __forceinline__ BlockRange block_range(const MaskInfoParams& p,
 // the (clipped) block; the allowed set is [lo, hi].
 __device__ __forceinline__ int base_class(const MaskInfoParams& p,
                                           const BlockRange& br) {
-  const int lo = (p.flags & BSM_MASK_CAUSAL) ? 0 : kNegInf;
+  const int lo = (p.flags & BSM_MASK_CAUSAL) ? 0
+                 : (p.flags & BSM_MASK_BAND) ? 1 - p.window
+                                             : kNegInf;
   const int hi = (p.flags & BSM_MASK_LOCAL) ? p.window - 1 : kPosInf;
   const int dmin = br.r0 - br.c1, dmax = br.r1 - br.c0;
   if (dmax < lo || dmin > hi) return 0;
@@ -102,6 +104,7 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
   bool v = true;
   if (p.flags & BSM_MASK_CAUSAL) v = v && (k <= q);
   if (p.flags & BSM_MASK_LOCAL) v = v && (q - k < p.window);
+  if (p.flags & BSM_MASK_BAND) v = v && (k - q < p.window);
   return v;
 }
 
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(kMiThreads)
             hi = min(br.c1, sr_s[q - br.r0].y);
         if (p.flags & BSM_MASK_CAUSAL) hi = min(hi, q);
         if (p.flags & BSM_MASK_LOCAL) lo = max(lo, q - p.window + 1);
+        if (p.flags & BSM_MASK_BAND) hi = min(hi, q + p.window - 1);
         const int n = hi >= lo ? hi - lo + 1 : 0;
         any |= n > 0;
         all &= n == p.bkv;

@@ -15,6 +15,7 @@ import numpy as np
 MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
+MASK_BAND = 8
 
 
 def _rows_range(flags, window, Sq, Skv):
@@ -23,8 +24,10 @@ def _rows_range(flags, window, Sq, Skv):
     hi = np.full(Sq, Skv - 1, dtype=np.int64)
     if flags & MASK_CAUSAL:
         hi = np.minimum(hi, q)
-    if flags & MASK_LOCAL:  # one-sided: q - k < window
+    if flags & MASK_LOCAL:  # q - k < window
         lo = np.maximum(lo, q - window + 1)
+    if flags & MASK_BAND:  # and k - q < window
+        hi = np.minimum(hi, q + window - 1)
     return lo, hi
 
 

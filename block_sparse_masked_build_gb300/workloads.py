@@ -33,6 +33,7 @@ import torch
 MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
+MASK_BAND = 8
 
 SCORE_SOFTMAX = 0
 SCORE_POINTWISE = 1

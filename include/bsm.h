@@ -53,11 +53,16 @@ typedef enum bsm_score {
  * pointwise_splash_attention: MaskType.CAUSAL / FULL, segment ids).
  *   CAUSAL : key k visible from query q iff k <= q
  *   LOCAL  : iff q - k < window            (window >= 1)
+ *   BAND   : with LOCAL only, the window also bounds the keys after q:
+ *            iff k - q < window, so LOCAL|BAND is the symmetric sliding
+ *            window |q - k| < window (hstu_ops LocalMask((w, w)) with
+ *            MaskType.FULL)
  *   SEGMENT: iff q_segment_ids[b][q] == kv_segment_ids[b][k]
  * Elements past Sq or Skv (a ragged last block) are never visible. */
 #define BSM_MASK_CAUSAL 1u
 #define BSM_MASK_LOCAL 2u
 #define BSM_MASK_SEGMENT 4u
+#define BSM_MASK_BAND 8u
 
 typedef struct bsm_mask_spec {
   uint32_t flags;

@@ -21,6 +21,7 @@ special cases, invariants).
 """
 
 from .splash_oracle import (  # noqa: F401
+    MASK_BAND,
     MASK_CAUSAL,
     MASK_LOCAL,
     MASK_SEGMENT,

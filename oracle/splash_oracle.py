@@ -31,6 +31,7 @@ import numpy as np
 MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
+MASK_BAND = 8
 
 
 def _f64(x) -> np.ndarray:
@@ -50,8 +51,10 @@ def visible(flags, window, qi, ki, Sq, Skv, q_seg=None, kv_seg=None):
 
     Causal: k <= q (CausalMask, offset 0; hstu_ops ``pointwise_splash_attention``
     MaskType.CAUSAL).  Local: q - k < window (the local-window workload's
-    "(q-k) < 4096").  Segment: q_seg[q] == kv_seg[k] (hstu_ops ``_apply_mask``).
-    Full mask: every in-range element (MaskType.FULL).
+    "(q-k) < 4096").  Band (with local): also k - q < window, the symmetric
+    window of hstu_ops ``LocalMask((w, w))``.  Segment: q_seg[q] == kv_seg[k]
+    (hstu_ops ``_apply_mask``).  Full mask: every in-range element
+    (MaskType.FULL).
     """
     qi = np.asarray(qi)
     ki = np.asarray(ki)
@@ -60,6 +63,8 @@ def visible(flags, window, qi, ki, Sq, Skv, q_seg=None, kv_seg=None):
         vis = vis & (ki <= qi)
     if flags & MASK_LOCAL:
         vis = vis & ((qi - ki) < window)
+    if flags & MASK_BAND:
+        vis = vis & ((ki - qi) < window)
     if flags & MASK_SEGMENT:
         qs = np.asarray(q_seg)[np.clip(qi, 0, Sq - 1)]
         ks = np.asarray(kv_seg)[np.clip(ki, 0, Skv - 1)]

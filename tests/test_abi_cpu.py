@@ -75,7 +75,8 @@ def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
 
 @pytest.mark.parametrize("flags,window,bq,bkv,Sq", [
     (1, 0, 100, 128, 256), (1, 0, 8, 128, 256), (1, 0, 128, 1024, 256),
-    (2, 0, 128, 128, 256), (8, 0, 128, 128, 256), (1, 0, 128, 128, -1)])
+    (2, 0, 128, 128, 256), (8, 0, 128, 128, 256), (1, 0, 128, 128, -1),
+    (16, 0, 128, 128, 256)])
 def test_mask_info_bytes_rejects(lib, flags, window, bq, bkv, Sq):
     spec = MaskSpec(flags, window)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), 1, Sq, 256, bq,

@@ -20,7 +20,8 @@ from gpu_helpers import compare_lse, compare_out, run_gpu, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
-C, L, SG = bsm.MASK_CAUSAL, bsm.MASK_LOCAL, bsm.MASK_SEGMENT
+C, L, SG, BD = (bsm.MASK_CAUSAL, bsm.MASK_LOCAL, bsm.MASK_SEGMENT,
+                 bsm.MASK_BAND)
 SM, PW = bsm.SCORE_SOFTMAX, bsm.SCORE_POINTWISE
 
 
@@ -74,6 +75,12 @@ SMALL = [
     ("long_local_pingpong", 1, 1, 1, 4500, 4500, 128, C | L, 1500, SM, 128,
      128),
     ("long_pointwise_pingpong", 1, 1, 1, 4096, 4096, 128, C, 0, PW, 128, 128),
+    # symmetric sliding window |q - k| < W
+    ("band_softmax", 1, 2, 2, 700, 700, 128, L | BD, 150, SM, 128, 128),
+    ("band_ragged_b64", 1, 1, 1, 333, 333, 64, L | BD, 40, SM, 64, 64),
+    ("band_pointwise", 1, 2, 2, 640, 640, 128, L | BD, 200, PW, 128, 128),
+    ("band_long_pingpong", 1, 1, 1, 4224, 4224, 128, L | BD, 700, SM, 128,
+     128),
 ]
 
 
@@ -84,6 +91,13 @@ def test_small_cases_elementwise(case):
                    sigma=0.5 if score == PW else 1.0)
     _check_full(q, k, v, flags, window, None, None, 1 / math.sqrt(D), score,
                 block_q=bq, block_kv=bkv)
+
+
+def test_symmetric_window_with_segments_elementwise():
+    B, H, S, D = 2, 2, 900, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=17)
+    seg = wl.random_segment_ids(B, S, 50, 400, 18)
+    _check_full(q, k, v, L | BD | SG, 120, seg, seg, 0.1, SM)
 
 
 @pytest.mark.parametrize("score", [SM, PW])

@@ -107,6 +107,28 @@ def test_random_tiny_mask_info_bit_exact(n, flags, window, bq, bkv, Sq, Skv, B):
     _check_super_order(got, ref, T, -(-Sq // bq), bq, Sq)
 
 
+BAND_CASES = []
+_rng_b = np.random.default_rng(78)
+for _n in range(16):
+    _bq = int(_rng_b.choice([16, 32, 64, 128, 256]))
+    _bkv = int(_rng_b.choice([16, 32, 64, 128, 256]))
+    _S = int(_rng_b.integers(1, 700))
+    BAND_CASES.append((_n, 2 | 8 | (4 if _n % 4 == 3 else 0),
+                       int(_rng_b.integers(1, 300)), _bq, _bkv, _S,
+                       int(_rng_b.integers(1, 3))))
+
+
+@pytest.mark.parametrize("n,flags,window,bq,bkv,S,B", BAND_CASES)
+def test_symmetric_window_mask_info_bit_exact(n, flags, window, bq, bkv, S,
+                                              B):
+    seg = None
+    if flags & 4:
+        seg = wl.random_segment_ids(B, S, 3, 90, 500 + n)
+    ref = oracle.mask_info(flags, window, seg, seg, B, S, S, bq, bkv)
+    got = _gpu_info(flags, window, seg, seg, B, S, S, bq, bkv)
+    _assert_same(got, ref)
+
+
 def test_super_order_absent_above_limit():
     # 9 tables x 1024 super-tiles exceed the 8192-pair table: no order, and
     # the forward falls back to taking the last super-tiles first

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import MASK_CAUSAL, MASK_LOCAL, MASK_SEGMENT
+from oracle import MASK_BAND, MASK_CAUSAL, MASK_LOCAL, MASK_SEGMENT
 from block_sparse_masked_build_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -28,7 +28,8 @@ def _interval_classes(flags, window, Sq, Skv, bq, bkv):
     iff it lies inside it and the block is not cut by the sequence end.
     """
     nq, nk = -(-Sq // bq), -(-Skv // bkv)
-    lo_ok = 0 if flags & MASK_CAUSAL else -10**9
+    lo_ok = 0 if flags & MASK_CAUSAL else (
+        1 - window if flags & MASK_BAND else -10**9)
     hi_ok = (window - 1) if flags & MASK_LOCAL else 10**9
     cls = np.zeros((nq, nk), dtype=np.int8)
     for i in range(nq):
@@ -51,7 +52,8 @@ def _interval_classes(flags, window, Sq, Skv, bq, bkv):
 @pytest.mark.parametrize("flags,window", [
     (MASK_CAUSAL, 0), (MASK_CAUSAL | MASK_LOCAL, 200),
     (MASK_CAUSAL | MASK_LOCAL, 64), (MASK_CAUSAL | MASK_LOCAL, 1), (0, 0),
-    (MASK_LOCAL, 150)])
+    (MASK_LOCAL, 150), (MASK_LOCAL | MASK_BAND, 150),
+    (MASK_LOCAL | MASK_BAND, 1), (MASK_LOCAL | MASK_BAND, 64)])
 def test_classes_match_interval_derivation(Sq, Skv, bq, bkv, flags, window):
     mi = oracle.mask_info(flags, window, None, None, 1, Sq, Skv, bq, bkv)
     ref = _interval_classes(flags, window, Sq, Skv, bq, bkv)
@@ -149,6 +151,32 @@ def test_visible_pair_closed_forms():
     assert oracle.visible_pair_count(MASK_CAUSAL | MASK_SEGMENT, 0, seg, seg,
                                      1, sum(lens), sum(lens)) == \
         sum(n * (n + 1) // 2 for n in lens)
+
+
+def test_band_window_closed_forms():
+    # |q - k| < W: row q sees min(q, W-1) + min(S-1-q, W-1) + 1 keys
+    for S, W in [(1000, 1), (1000, 37), (4096, 512), (300, 5000)]:
+        want = sum(min(q, W - 1) + min(S - 1 - q, W - 1) + 1
+                   for q in range(S))
+        assert oracle.visible_pair_count(MASK_LOCAL | MASK_BAND, W, None,
+                                         None, 1, S, S) == want
+    # square blocks of size b with W = b: row i has blocks i-1, i, i+1; the
+    # diagonal block is full (|q - k| <= b-1 < W there), its neighbours
+    # partial (each holds the pair |q - k| = b)
+    S, b = 1024, 128
+    nq = S // b
+    mi = oracle.mask_info(MASK_LOCAL | MASK_BAND, b, None, None, 1, S, S, b, b)
+    bm = mi["block_mask"][0]
+    assert int((bm > 0).sum()) == 3 * nq - 2
+    assert int((bm == 2).sum()) == nq
+    np.testing.assert_array_equal(np.diag(bm), np.full(nq, 2))
+    # the band is symmetric; with causal it adds nothing
+    vis = oracle.visibility_matrix(MASK_LOCAL | MASK_BAND, 9, 60, 60)
+    np.testing.assert_array_equal(vis, vis.T)
+    a = oracle.visibility_matrix(MASK_CAUSAL | MASK_LOCAL | MASK_BAND, 9, 60,
+                                 60)
+    np.testing.assert_array_equal(
+        a, oracle.visibility_matrix(MASK_CAUSAL | MASK_LOCAL, 9, 60, 60))
 
 
 def _read_golden():

@@ -124,6 +124,18 @@ def test_local_window_matches_sdpa_band_mask():
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
 
 
+def test_symmetric_window_matches_sdpa_band_mask():
+    # |q - k| < W  ==  np.triu(., -(W-1)) & np.tril(., W-1)
+    B, H, S, D, W = 1, 2, 150, 32, 23
+    q, k, v = _qkv(B, H, S, S, D, 16)
+    flags = oracle.MASK_LOCAL | oracle.MASK_BAND
+    out, _ = oracle.softmax_attention(q, k, v, flags, W, None, None, 0.2)
+    ones = np.ones((S, S), dtype=bool)
+    band = np.tril(ones, W - 1) & np.triu(ones, -(W - 1))
+    ref = _sdpa64(q, k, v, band, 0.2)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
 def test_packed_segments_match_sdpa_block_diagonal_mask():
     B, H, D = 1, 2, 32
     lens = [17, 40, 3, 60, 30]
