@@ -7,6 +7,7 @@ ABI of ``include/bsm.h``; this package is its Python binding.
 from .api import (  # noqa: F401
     MASK_BAND,
     MASK_CAUSAL,
+    MASK_DENSE,
     MASK_LOCAL,
     MASK_SEGMENT,
     SCORE_POINTWISE,

@@ -30,7 +30,9 @@ STATUS_NAMES = {
 
 
 class MaskSpec(ctypes.Structure):
-    _fields_ = [("flags", ctypes.c_uint32), ("window", ctypes.c_int32)]
+    _fields_ = [("flags", ctypes.c_uint32), ("window", ctypes.c_int32),
+                ("dense_bits", ctypes.c_void_p),
+                ("dense_row_words", ctypes.c_int64)]
 
 
 class MaskInfoStruct(ctypes.Structure):
@@ -53,6 +55,8 @@ class MaskInfoStruct(ctypes.Structure):
         ("seg_flags", ctypes.c_void_p),
         ("num_super", ctypes.c_int32),
         ("super_order", ctypes.c_void_p),
+        ("dense_bits", ctypes.c_void_p),
+        ("dense_row_words", ctypes.c_int64),
     ]
 
 

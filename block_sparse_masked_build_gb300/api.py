@@ -21,6 +21,7 @@ MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
 MASK_BAND = 8  # with MASK_LOCAL: |q - k| < window
+MASK_DENSE = 16  # arbitrary mask, bit-packed uint32 words per query row
 SCORE_SOFTMAX = 0
 SCORE_POINTWISE = 1
 
@@ -72,6 +73,7 @@ class MaskInfo:
 
     struct: MaskInfoStruct
     buffer: torch.Tensor
+    dense_bits: object = None  # keeps a MASK_DENSE mask alive with the info
 
     def _view(self, ptr: int, dtype, count: int) -> torch.Tensor:
         off = ptr - self.buffer.data_ptr()
@@ -141,15 +143,26 @@ class MaskInfo:
 
 def bsm_build_mask_info(flags: int, window: int, q_segment_ids, kv_segment_ids,
                         B: int, Sq: int, Skv: int, block_q: int, block_kv: int,
-                        buffer: torch.Tensor, stream=None) -> MaskInfo:
+                        buffer: torch.Tensor, stream=None,
+                        dense_bits=None) -> MaskInfo:
+    """dense_bits: with MASK_DENSE, a device int32/uint32-bits tensor
+    [Sq, W] (W >= ceil(Skv / 32), row-major); it must stay alive while the
+    mask info is used, since the forward reads it too."""
     spec = MaskSpec(flags, window)
+    if dense_bits is not None:
+        if dense_bits.dim() != 2 or dense_bits.stride(1) != 1 or \
+                dense_bits.element_size() != 4:
+            raise ValueError("dense_bits must be a [Sq, W] 32-bit tensor with "
+                             "contiguous rows")
+        spec.dense_bits = dense_bits.data_ptr()
+        spec.dense_row_words = dense_bits.stride(0)
     info = MaskInfoStruct()
     _check(_lib.lib().bsm_build_mask_info(
         ctypes.byref(spec), _ptr(q_segment_ids), _ptr(kv_segment_ids), B, Sq,
         Skv, block_q, block_kv, buffer.data_ptr(),
         buffer.numel() * buffer.element_size(), ctypes.byref(info),
         _stream_handle(stream)))
-    return MaskInfo(info, buffer)
+    return MaskInfo(info, buffer, dense_bits)
 
 
 def _strides3(t: torch.Tensor):
@@ -262,7 +275,8 @@ def decode_trace(buffer, grid: int):
 
 def build_mask_info(flags: int, B: int, Sq: int, Skv: int, block_q: int = 128,
                     block_kv: int = 128, window: int = 0, q_segment_ids=None,
-                    kv_segment_ids=None, device=None, stream=None) -> MaskInfo:
+                    kv_segment_ids=None, device=None, stream=None,
+                    dense_bits=None) -> MaskInfo:
     """Allocate the mask-info buffer with torch and build the tables."""
     nbytes = bsm_mask_info_bytes(flags, window, B, Sq, Skv, block_q, block_kv)
     if nbytes == 0:
@@ -272,7 +286,8 @@ def build_mask_info(flags: int, B: int, Sq: int, Skv: int, block_q: int = 128,
                   else torch.device("cuda"))
     buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
     return bsm_build_mask_info(flags, window, q_segment_ids, kv_segment_ids, B,
-                               Sq, Skv, block_q, block_kv, buf, stream)
+                               Sq, Skv, block_q, block_kv, buf, stream,
+                               dense_bits)
 
 
 def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,

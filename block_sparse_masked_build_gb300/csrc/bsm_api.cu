@@ -71,8 +71,8 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows,
 
 bsm_status check_spec(const bsm_mask_spec* spec) {
   if (spec == nullptr) return fail(BSM_ERR_INVALID_ARG, "mask spec is NULL");
-  const uint32_t known =
-      BSM_MASK_CAUSAL | BSM_MASK_LOCAL | BSM_MASK_SEGMENT | BSM_MASK_BAND;
+  const uint32_t known = BSM_MASK_CAUSAL | BSM_MASK_LOCAL | BSM_MASK_SEGMENT |
+                         BSM_MASK_BAND | BSM_MASK_DENSE;
   if (spec->flags & ~known)
     return fail(BSM_ERR_INVALID_ARG, "unknown mask flag bits");
   if ((spec->flags & BSM_MASK_BAND) && !(spec->flags & BSM_MASK_LOCAL))
@@ -217,6 +217,12 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
     return fail(BSM_ERR_INVALID_ARG,
                 "segment ids given without BSM_MASK_SEGMENT");
   if (seg && B < 1) return fail(BSM_ERR_INVALID_ARG, "B must be >= 1");
+  const bool dense = (spec->flags & BSM_MASK_DENSE) != 0;
+  if (dense && (spec->dense_bits == nullptr ||
+                spec->dense_row_words < (static_cast<int64_t>(Skv) + 31) / 32))
+    return fail(BSM_ERR_INVALID_ARG,
+                "BSM_MASK_DENSE needs dense_bits and dense_row_words >= "
+                "ceil(Skv / 32)");
   const int64_t tables = seg ? B : 1;
   const int64_t nq = (Sq + block_q - 1) / block_q;
   const int64_t nk = (Skv + block_kv - 1) / block_kv;
@@ -254,6 +260,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   mi.seg_range = reinterpret_cast<int32_t*>(base + L.off_sr);
   mi.seg_flags = reinterpret_cast<int32_t*>(base + L.off_sf);
   mi.num_super = static_cast<int32_t>((Sq + bsm::kUnitRows - 1) / bsm::kUnitRows);
+  mi.dense_bits = dense ? spec->dense_bits : nullptr;
+  mi.dense_row_words = dense ? spec->dense_row_words : 0;
   mi.super_order = pairs <= bsm::kMaxSuperOrder
                        ? reinterpret_cast<int32_t*>(base + L.off_so)
                        : nullptr;
@@ -279,6 +287,8 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   p.seg_flags = mi.seg_flags;
   p.n_super = mi.num_super;
   p.super_order = mi.super_order;
+  p.dense = mi.dense_bits;
+  p.dense_words = mi.dense_row_words;
   cudaError_t e =
       bsm::launch_mask_info(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mask-info launch");
@@ -332,6 +342,10 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   if (!seg && (q_segment_ids != nullptr || kv_segment_ids != nullptr))
     return fail(BSM_ERR_INVALID_ARG,
                 "segment ids given without BSM_MASK_SEGMENT");
+  if ((info->flags & BSM_MASK_DENSE) &&
+      (info->dense_bits == nullptr ||
+       info->dense_row_words < (static_cast<int64_t>(Skv) + 31) / 32))
+    return fail(BSM_ERR_INVALID_ARG, "mask info lacks its dense mask");
   if (seg && (info->seg_range == nullptr || info->seg_flags == nullptr))
     return fail(BSM_ERR_INVALID_ARG, "mask info lacks segment ranges");
   const int64_t n_super = (Sq + bsm::kUnitRows - 1) / bsm::kUnitRows;
@@ -400,6 +414,8 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   p.seg_range = info->seg_range;
   p.seg_flags = info->seg_flags;
   p.super_order = info->super_order;
+  p.dense = (info->flags & BSM_MASK_DENSE) ? info->dense_bits : nullptr;
+  p.dense_words = info->dense_row_words;
   p.score = score;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.scale = scale;

@@ -597,9 +597,10 @@ __device__ __forceinline__ void mask_tile(float* s, int lo_c, int hi_c,
   }
 }
 
-// SEG_ELEM: segment ids are compared element by element (some key-id row is
-// not sorted); otherwise every mask is a key range per row.
-template <int D, int SCORE, bool SEG_ELEM, bool PINGPONG>
+// KEEP: partial tiles also carry per-element "keep" bits -- from segment ids
+// compared element by element (some key-id row is not sorted) and/or from
+// an arbitrary bit-packed mask; otherwise every mask is a key range per row.
+template <int D, int SCORE, bool KEEP, bool PINGPONG>
 __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
                                            const uint16_t* lists,
                                            uint32_t tmem) {
@@ -614,7 +615,8 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
   volatile int* abort_flag = &bars->abort;
   const float NEG_INF = __int_as_float(0xff800000);
   const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
-  constexpr bool seg_elem = SEG_ELEM;
+  const bool seg_elem = KEEP && seg && (*p.seg_flags & 1) != 0;
+  const bool dense = KEEP && p.dense != nullptr;
   uint32_t s_cnt = 0, pv_cnt = 0, turns = 0;
   auto pass_turn = [&]() {
     __syncwarp();
@@ -684,8 +686,19 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
       const int jt = static_cast<int>(ent >> 4);
       const int kbase = jt * kTileN;
       uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (SEG_ELEM && cls == 1)
-        segment_bits(keep, segk_b + kbase, min(kTileN, p.Skv - kbase), segq);
+      if (KEEP && cls == 1) {
+        if (seg_elem)
+          segment_bits(keep, segk_b + kbase, min(kTileN, p.Skv - kbase), segq);
+        if (dense) {  // the row's mask words for these 128 keys
+          const int64_t w0 = kbase >> 5;
+          const uint32_t* dw =
+              p.dense + static_cast<int64_t>(row_ok ? qrow : 0) * p.dense_words;
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            keep[w] &= (row_ok && w0 + w < p.dense_words) ? __ldg(dw + w0 + w)
+                                                          : 0u;
+        }
+      }
       ok = warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, p.timeout_ns);
       if (!ok) {
         record_timeout(kRoleScore, 1);
@@ -700,7 +713,7 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         tmem_ld32(s_addr + q * 32, sraw + q * 32);
       tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sraw);
-      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep, seg_elem);
+      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep, KEEP);
 
       uint32_t pk[16];
       if (SCORE == BSM_SCORE_SOFTMAX) {
@@ -920,9 +933,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_role<D>(p, smem, bars, lists, tmem, warp - 1);
   } else {
     setmaxnreg_inc<kRegsScore>();
-    // one path per launch: the element-wise segment compare only when a
-    // key-id row is unsorted (read once; the same for every thread)
-    if ((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0)
+    // one path per launch: per-element keep bits only when segment ids are
+    // unsorted or an arbitrary mask is given (read once; the same for every
+    // thread)
+    if (((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0) ||
+        p.dense != nullptr)
       score_role<D, SCORE, true, PINGPONG>(p, bars, lists, tmem);
     else
       score_role<D, SCORE, false, PINGPONG>(p, bars, lists, tmem);

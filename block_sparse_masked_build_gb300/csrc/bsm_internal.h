@@ -42,12 +42,16 @@ struct MaskInfoParams {
   int32_t* seg_flags;  // [1]: bit 0 = some kv id row is not sorted
   int32_t n_super;        // ceil(Sq / kUnitRows)
   int32_t* super_order;   // [tables * n_super] or null
+  const uint32_t* dense;  // DENSE: [Sq][dense_words] bit-packed, else null
+  int64_t dense_words;
 };
 
 struct FwdParams {
   int32_t B, H, Hkv, Sq, Skv, D;
   int32_t n_super;    // ceil(Sq / 256)
   const int32_t* super_order;  // longest-first (table, super-tile) or null
+  const uint32_t* dense;       // DENSE: [Sq][dense_words] bit-packed, else null
+  int64_t dense_words;
   int32_t n_kvtiles;  // ceil(Skv / 128)
   int32_t num_units;  // B * H * n_super
   // mask

@@ -34,6 +34,7 @@ MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
 MASK_BAND = 8
+MASK_DENSE = 16
 
 SCORE_SOFTMAX = 0
 SCORE_POINTWISE = 1
@@ -191,3 +192,36 @@ def sample_rows(w: Workload, n: int, seed: int, seg: np.ndarray | None = None):
     for p in picks:
         rows.add(p)
     return sorted(rows)
+
+
+def random_dense_mask(Sq: int, Skv: int, p_visible: float, block: int,
+                      seed: int) -> np.ndarray:
+    """Seeded boolean [Sq, Skv] mask for the arbitrary-mask path: each
+    block x block tile is empty, full or random (visible with probability
+    p_visible) with equal odds, so every block class occurs."""
+    rng = np.random.default_rng(seed)
+    m = rng.random((Sq, Skv)) < p_visible
+    nq, nk = -(-Sq // block), -(-Skv // block)
+    kind = rng.integers(0, 3, size=(nq, nk))
+    for i in range(nq):
+        for j in range(nk):
+            sl = (slice(i * block, (i + 1) * block),
+                  slice(j * block, (j + 1) * block))
+            if kind[i, j] == 0:
+                m[sl] = False
+            elif kind[i, j] == 1:
+                m[sl] = True
+    return m
+
+
+def pack_dense_mask(mask: np.ndarray, row_words: int = 0) -> np.ndarray:
+    """Bit-pack a boolean [Sq, Skv] mask into uint32 words, row-major: bit
+    k % 32 of word k // 32 of row q is mask[q, k].  row_words (>= the
+    minimum ceil(Skv / 32)) pads each row."""
+    Sq, Skv = mask.shape
+    w = max(row_words, -(-Skv // 32))
+    padded = np.zeros((Sq, w * 32), dtype=bool)
+    padded[:, :Skv] = mask
+    bits = padded.reshape(Sq, w, 32).astype(np.uint64)
+    words = (bits << np.arange(32, dtype=np.uint64)).sum(axis=2)
+    return words.astype(np.uint32)

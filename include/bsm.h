@@ -58,15 +58,24 @@ typedef enum bsm_score {
  *            window |q - k| < window (hstu_ops LocalMask((w, w)) with
  *            MaskType.FULL)
  *   SEGMENT: iff q_segment_ids[b][q] == kv_segment_ids[b][k]
+ *   DENSE  : iff bit k % 32 of word dense_bits[q * dense_row_words + k / 32]
+ *            is set: an arbitrary mask ([HSTU]'s NumpyMask), bit-packed,
+ *            one row of dense_row_words >= ceil(Skv / 32) uint32 words per
+ *            query row, shared by every batch row and head; device memory
+ *            owned by the caller, read by bsm_build_mask_info and again by
+ *            bsm_splash_fwd (keep it alive while the mask info is used)
  * Elements past Sq or Skv (a ragged last block) are never visible. */
 #define BSM_MASK_CAUSAL 1u
 #define BSM_MASK_LOCAL 2u
 #define BSM_MASK_SEGMENT 4u
 #define BSM_MASK_BAND 8u
+#define BSM_MASK_DENSE 16u
 
 typedef struct bsm_mask_spec {
   uint32_t flags;
   int32_t window;  /* used with BSM_MASK_LOCAL only */
+  const uint32_t* dense_bits; /* BSM_MASK_DENSE only, else NULL */
+  int64_t dense_row_words;    /* BSM_MASK_DENSE only */
 } bsm_mask_spec;
 
 /* Mask-info tables ([HSTU] _next_nonzero; [NOTES] section 21), filled by
@@ -116,6 +125,8 @@ typedef struct bsm_mask_info {
   int32_t* seg_flags;
   int32_t num_super; /* ceil(Sq / 256) */
   int32_t* super_order;
+  const uint32_t* dense_bits; /* the spec's, for the forward (DENSE only) */
+  int64_t dense_row_words;
 } bsm_mask_info;
 
 /* Bytes the caller must allocate for bsm_build_mask_info (0 on bad

@@ -23,6 +23,7 @@ special cases, invariants).
 from .splash_oracle import (  # noqa: F401
     MASK_BAND,
     MASK_CAUSAL,
+    MASK_DENSE,
     MASK_LOCAL,
     MASK_SEGMENT,
     visible,

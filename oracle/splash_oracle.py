@@ -32,6 +32,7 @@ MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
 MASK_BAND = 8
+MASK_DENSE = 16
 
 
 def _f64(x) -> np.ndarray:
@@ -46,14 +47,16 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def visible(flags, window, qi, ki, Sq, Skv, q_seg=None, kv_seg=None):
+def visible(flags, window, qi, ki, Sq, Skv, q_seg=None, kv_seg=None,
+            dense=None):
     """Per-element visibility (broadcasts qi against ki).
 
     Causal: k <= q (CausalMask, offset 0; hstu_ops ``pointwise_splash_attention``
     MaskType.CAUSAL).  Local: q - k < window (the local-window workload's
     "(q-k) < 4096").  Band (with local): also k - q < window, the symmetric
     window of hstu_ops ``LocalMask((w, w))``.  Segment: q_seg[q] == kv_seg[k]
-    (hstu_ops ``_apply_mask``).  Full mask: every in-range element
+    (hstu_ops ``_apply_mask``).  Dense: an arbitrary boolean [Sq, Skv] mask,
+    dense[q, k] (hstu_ops ``NumpyMask``).  Full mask: every in-range element
     (MaskType.FULL).
     """
     qi = np.asarray(qi)
@@ -69,19 +72,22 @@ def visible(flags, window, qi, ki, Sq, Skv, q_seg=None, kv_seg=None):
         qs = np.asarray(q_seg)[np.clip(qi, 0, Sq - 1)]
         ks = np.asarray(kv_seg)[np.clip(ki, 0, Skv - 1)]
         vis = vis & (qs == ks)
+    if flags & MASK_DENSE:
+        dm = np.asarray(dense, dtype=bool)
+        vis = vis & dm[np.clip(qi, 0, Sq - 1), np.clip(ki, 0, Skv - 1)]
     return vis
 
 
 def visibility_matrix(flags, window, Sq, Skv, q_seg=None, kv_seg=None,
-                      rows=None):
+                      rows=None, dense=None):
     """Boolean [len(rows), Skv] visibility for one batch row's segment ids."""
     qi = np.arange(Sq) if rows is None else np.asarray(rows)
     ki = np.arange(Skv)
     return visible(flags, window, qi[:, None], ki[None, :], Sq, Skv,
-                   q_seg, kv_seg)
+                   q_seg, kv_seg, dense)
 
 
-def mask_info(flags, window, q_seg, kv_seg, B, Sq, Skv, bq, bkv):
+def mask_info(flags, window, q_seg, kv_seg, B, Sq, Skv, bq, bkv, dense=None):
     """Brute-force mask-info by an exact per-element scan of every block.
 
     Class encoding from hstu_ops ``_next_nonzero``: 0 = empty (block not
@@ -110,7 +116,7 @@ def mask_info(flags, window, q_seg, kv_seg, B, Sq, Skv, bq, bkv):
         for i in range(nq):
             rows = np.arange(i * bq, (i + 1) * bq)
             vis = visible(flags, window, rows[:, None], cols[None, :], Sq, Skv,
-                          qs, ks)
+                          qs, ks, dense)
             cnt = vis.reshape(bq, nk, bkv).sum(axis=(0, 2))
             cls = np.where(cnt == 0, 0, np.where(cnt == bq * bkv, 2, 1))
             block_mask[b, i] = cls
@@ -135,7 +141,8 @@ def mask_info(flags, window, q_seg, kv_seg, B, Sq, Skv, bq, bkv):
     }
 
 
-def visible_pair_count(flags, window, q_seg, kv_seg, B, Sq, Skv, slab=1024):
+def visible_pair_count(flags, window, q_seg, kv_seg, B, Sq, Skv, slab=1024,
+                       dense=None):
     """Number of visible (q, k) pairs summed over batch rows (per head)."""
     total = 0
     for b in range(B):
@@ -144,7 +151,7 @@ def visible_pair_count(flags, window, q_seg, kv_seg, B, Sq, Skv, slab=1024):
         for r0 in range(0, Sq, slab):
             rows = np.arange(r0, min(Sq, r0 + slab))
             total += int(visibility_matrix(flags, window, Sq, Skv, qs, ks,
-                                           rows).sum())
+                                           rows, dense).sum())
     return total
 
 
@@ -169,7 +176,7 @@ def _row_groups(B, H, Sq, rows):
 
 
 def softmax_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
-                      rows=None, slab=512):
+                      rows=None, slab=512, dense=None):
     """Masked softmax attention, materialised, two passes per row.
 
     Splash notes section 12 (naive attention: scores = Q K^T, mask, row max,
@@ -198,7 +205,7 @@ def softmax_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
         for s0 in range(0, len(qrows), slab):
             rr = qrows[s0:s0 + slab]
             a = scale * (qf[b, h, rr] @ kf[b, h].T)          # [r, Skv]
-            vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, rr)
+            vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, rr, dense)
             a = np.where(vis, a, -np.inf)
             M = a.max(axis=1)                                 # [r]
             any_vis = vis.any(axis=1)
@@ -222,7 +229,7 @@ def softmax_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
 
 
 def softmax_attention_online(q, k, v, flags, window, q_seg, kv_seg, scale,
-                             block_kv, b=0, h=0):
+                             block_kv, b=0, h=0, dense=None):
     """Online softmax over KV blocks of ``block_kv`` keys for one (b, h).
 
     Splash notes section 15.1-15.3: per block B, m_new = max(m, max_B a);
@@ -244,7 +251,7 @@ def softmax_attention_online(q, k, v, flags, window, q_seg, kv_seg, scale,
         cols = np.arange(j0, min(Skv, j0 + block_kv))
         a = scale * (qf @ kf[cols].T)
         vis = visible(flags, window, rows[:, None], cols[None, :], Sq, Skv,
-                      qs, ks)
+                      qs, ks, dense)
         a = np.where(vis, a, -np.inf)
         m_new = np.maximum(m, a.max(axis=1))
         alive = np.isfinite(m_new)
@@ -266,7 +273,7 @@ def _silu(x):
 
 
 def pointwise_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
-                        rows=None, slab=512):
+                        rows=None, slab=512, dense=None):
     """Pointwise (HSTU) attention, materialised.
 
     hstu_ops ``_pointwise_splash_attention_fwd_kernel_impl``: qk = q . k (f32
@@ -290,7 +297,7 @@ def pointwise_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
             rr = qrows[s0:s0 + slab]
             x = scale * (qf[b, h, rr] @ kf[b, h].T)
             p = _silu(x) * (1.0 / Sq)
-            vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, rr)
+            vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, rr, dense)
             p = np.where(vis, p, 0.0)
             o = p @ vf[b, h]
             if rows is None:

@@ -25,8 +25,15 @@ PW_MAX_REL = 2e-2
 PW_MEAN_REL = 2.0 ** -8
 
 
+def dense_device_bits(dense, row_words=0):
+    """Bit-packed device copy of a boolean [Sq, Skv] mask (int32 view)."""
+    words = wl.pack_dense_mask(np.asarray(dense, dtype=bool), row_words)
+    return torch.from_numpy(words.view(np.int32)).to("cuda")
+
+
 def run_gpu(q, k, v, flags, window, q_seg, kv_seg, scale, score,
-            block_q=128, block_kv=128, layout="bhsd", longest_first=True):
+            block_q=128, block_kv=128, layout="bhsd", longest_first=True,
+            dense=None, dense_row_words=0):
     """Run mask-info build + forward on the GPU; returns CPU out, lse, info.
     longest_first=False drops the mask info's unit order, so the forward
     takes its fallback schedule."""
@@ -40,8 +47,9 @@ def run_gpu(q, k, v, flags, window, q_seg, kv_seg, scale, score,
     ks = None if kv_seg is None else torch.from_numpy(np.ascontiguousarray(kv_seg)).to(dev)
     B, H, Sq, D = q.shape
     Skv = k.shape[2]
+    db = None if dense is None else dense_device_bits(dense, dense_row_words)
     info = bsm.build_mask_info(flags, B, Sq, Skv, block_q, block_kv, window,
-                               qs, ks, device=dev)
+                               qs, ks, device=dev, dense_bits=db)
     out = torch.full((B, H, Sq, D), float("nan"), dtype=torch.bfloat16,
                      device=dev)
     if layout == "bshd":

@@ -76,7 +76,7 @@ def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
 @pytest.mark.parametrize("flags,window,bq,bkv,Sq", [
     (1, 0, 100, 128, 256), (1, 0, 8, 128, 256), (1, 0, 128, 1024, 256),
     (2, 0, 128, 128, 256), (8, 0, 128, 128, 256), (1, 0, 128, 128, -1),
-    (16, 0, 128, 128, 256)])
+    (32, 0, 128, 128, 256)])
 def test_mask_info_bytes_rejects(lib, flags, window, bq, bkv, Sq):
     spec = MaskSpec(flags, window)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), 1, Sq, 256, bq,
@@ -88,6 +88,19 @@ def _build(lib, spec, qs, ks, B, Sq, Skv, bq, bkv, buf, nbytes):
     return lib.bsm_build_mask_info(
         None if spec is None else ctypes.byref(spec), qs, ks, B, Sq, Skv, bq,
         bkv, buf, nbytes, ctypes.byref(info), None)
+
+
+def test_dense_mask_needs_its_bits(lib):
+    # an arbitrary mask without its bit array, or with rows shorter than
+    # ceil(Skv / 32) words, is rejected before any device work
+    spec = MaskSpec(16, 0)
+    assert _build(lib, spec, None, None, 1, 256, 256, 64, 64, 0x100000,
+                  1 << 20) == INVALID
+    assert "dense" in _lib.last_error()
+    spec.dense_bits = 0x200000
+    spec.dense_row_words = 7  # 256 keys need 8 words
+    assert _build(lib, spec, None, None, 1, 256, 256, 64, 64, 0x100000,
+                  1 << 20) == INVALID
 
 
 def test_build_mask_info_argument_errors(lib):

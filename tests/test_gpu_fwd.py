@@ -20,8 +20,8 @@ from gpu_helpers import compare_lse, compare_out, run_gpu, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
-C, L, SG, BD = (bsm.MASK_CAUSAL, bsm.MASK_LOCAL, bsm.MASK_SEGMENT,
-                 bsm.MASK_BAND)
+C, L, SG, BD, DN = (bsm.MASK_CAUSAL, bsm.MASK_LOCAL, bsm.MASK_SEGMENT,
+                     bsm.MASK_BAND, bsm.MASK_DENSE)
 SM, PW = bsm.SCORE_SOFTMAX, bsm.SCORE_POINTWISE
 
 
@@ -42,14 +42,15 @@ def _check_full(q, k, v, flags, window, sq, skv, scale, score, **kw):
     out, lse, _ = run_gpu(q, k, v, flags, window, sq, skv, scale, score, **kw)
     H = q.shape[1]
     ke, ve = _expand_kv(k, H), _expand_kv(v, H)
+    dense = kw.get("dense")
     if score == SM:
         ref, ref_lse = oracle.softmax_attention(q, ke, ve, flags, window, sq,
-                                                skv, scale)
+                                                skv, scale, dense=dense)
         compare_out(out.numpy(), ref, what="softmax")
         compare_lse(lse.numpy(), ref_lse, what="lse")
     else:
         ref = oracle.pointwise_attention(q, ke, ve, flags, window, sq, skv,
-                                         scale)
+                                         scale, dense=dense)
         compare_out(out.numpy(), ref, pointwise=True, what="pointwise")
     return out, lse
 
@@ -91,6 +92,30 @@ def test_small_cases_elementwise(case):
                    sigma=0.5 if score == PW else 1.0)
     _check_full(q, k, v, flags, window, None, None, 1 / math.sqrt(D), score,
                 block_q=bq, block_kv=bkv)
+
+
+@pytest.mark.parametrize("score", [SM, PW])
+@pytest.mark.parametrize("extra", [0, C])
+def test_dense_mask_elementwise(score, extra):
+    # an arbitrary bit-packed mask (empty, full and random 64x64 tiles),
+    # alone or with causal, ragged at both ends
+    B, H, Sq, Skv, D = 2, 2, 700 if extra else 500, 700 if extra else 650, 128
+    q, k, v = _qkv(B, H, H, Sq, Skv, D, seed=22,
+                   sigma=0.5 if score == PW else 1.0)
+    dm = wl.random_dense_mask(Sq, Skv, 0.3, 64, 23)
+    _check_full(q, k, v, DN | extra, 0, None, None, 0.1, score, dense=dm,
+                dense_row_words=24)
+
+
+def test_dense_mask_with_segments_and_long_keys_elementwise():
+    # arbitrary mask AND packed segments; 4224 keys take the kernel whose
+    # score warps alternate turns
+    B, H, S, D = 1, 1, 4224, 128
+    q, k, v = _qkv(B, H, H, S, S, D, seed=24)
+    dm = wl.random_dense_mask(S, S, 0.5, 128, 25)
+    seg = wl.random_segment_ids(B, S, 500, 2000, 26)
+    _check_full(q, k, v, DN | SG | C, 0, seg, seg, 0.1, SM, dense=dm)
+    _check_full(q, k, v, DN | C, 0, None, None, 0.1, SM, dense=dm)
 
 
 def test_symmetric_window_with_segments_elementwise():

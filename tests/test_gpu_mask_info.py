@@ -7,16 +7,19 @@ import torch
 import oracle
 import block_sparse_masked_build_gb300 as bsm
 from block_sparse_masked_build_gb300 import workloads as wl
+from gpu_helpers import dense_device_bits
 
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv):
+def _gpu_info(flags, window, seg_q, seg_kv, B, Sq, Skv, bq, bkv, dense=None,
+              dense_row_words=0):
     dev = torch.device("cuda")
     qs = None if seg_q is None else torch.from_numpy(seg_q).to(dev)
     ks = None if seg_kv is None else torch.from_numpy(seg_kv).to(dev)
+    db = None if dense is None else dense_device_bits(dense, dense_row_words)
     info = bsm.build_mask_info(flags, B, Sq, Skv, bq, bkv, window, qs, ks,
-                               device=dev)
+                               device=dev, dense_bits=db)
     torch.cuda.synchronize()
     idx, cls = info.kv_lists()
     return {
@@ -126,6 +129,31 @@ def test_symmetric_window_mask_info_bit_exact(n, flags, window, bq, bkv, S,
         seg = wl.random_segment_ids(B, S, 3, 90, 500 + n)
     ref = oracle.mask_info(flags, window, seg, seg, B, S, S, bq, bkv)
     got = _gpu_info(flags, window, seg, seg, B, S, S, bq, bkv)
+    _assert_same(got, ref)
+
+
+DENSE_CASES = []
+_rng_d = np.random.default_rng(79)
+for _n in range(14):
+    _bq = int(_rng_d.choice([16, 32, 64, 128]))
+    _bkv = int(_rng_d.choice([16, 32, 64, 128]))
+    _Sq = int(_rng_d.integers(1, 600))
+    _extra = int(_rng_d.choice([0, 1, 2, 4]))  # +causal / local / segment
+    _Skv = _Sq if _extra else int(_rng_d.integers(1, 600))
+    DENSE_CASES.append((_n, 16 | _extra, int(_rng_d.integers(20, 200)), _bq,
+                        _bkv, _Sq, _Skv, int(_rng_d.integers(1, 3))))
+
+
+@pytest.mark.parametrize("n,flags,window,bq,bkv,Sq,Skv,B", DENSE_CASES)
+def test_dense_mask_info_bit_exact(n, flags, window, bq, bkv, Sq, Skv, B):
+    dm = wl.random_dense_mask(Sq, Skv, 0.35, int(min(bq, bkv)), 600 + n)
+    seg = None
+    if flags & 4:
+        seg = wl.random_segment_ids(B, Sq, 3, 90, 700 + n)
+    ref = oracle.mask_info(flags, window, seg, seg, B, Sq, Skv, bq, bkv,
+                           dense=dm)
+    got = _gpu_info(flags, window, seg, seg, B, Sq, Skv, bq, bkv, dense=dm,
+                    dense_row_words=n % 3)
     _assert_same(got, ref)
 
 

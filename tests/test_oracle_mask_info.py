@@ -179,6 +179,33 @@ def test_band_window_closed_forms():
         a, oracle.visibility_matrix(MASK_CAUSAL | MASK_LOCAL, 9, 60, 60))
 
 
+@pytest.mark.parametrize("Sq,Skv,bq,bkv,seed", [
+    (256, 256, 64, 64, 1), (300, 200, 32, 64, 2), (128, 520, 128, 128, 3),
+    (97, 97, 16, 32, 4)])
+def test_dense_mask_classes_from_block_counts(Sq, Skv, bq, bkv, seed):
+    # classes straight from the mask: pad it to whole blocks with False,
+    # count the set elements of each block by reshaping
+    dm = wl.random_dense_mask(Sq, Skv, 0.4, 32, seed)
+    nq, nk = -(-Sq // bq), -(-Skv // bkv)
+    pad = np.zeros((nq * bq, nk * bkv), dtype=bool)
+    pad[:Sq, :Skv] = dm
+    cnt = pad.reshape(nq, bq, nk, bkv).sum(axis=(1, 3))
+    want = np.where(cnt == 0, 0, np.where(cnt == bq * bkv, 2, 1))
+    mi = oracle.mask_info(oracle.MASK_DENSE, 0, None, None, 1, Sq, Skv, bq,
+                          bkv, dense=dm)
+    np.testing.assert_array_equal(mi["block_mask"][0], want)
+
+
+def test_dense_pack_round_trip():
+    dm = wl.random_dense_mask(70, 100, 0.5, 16, 9)
+    words = wl.pack_dense_mask(dm, row_words=5)
+    assert words.shape == (70, 5) and words.dtype == np.uint32
+    k = np.arange(100)
+    back = ((words[:, k // 32] >> (k % 32).astype(np.uint32)) & 1).astype(bool)
+    np.testing.assert_array_equal(back, dm)
+    assert not words[:, 4].any() and not (words[:, 3] >> 4).any()
+
+
 def _read_golden():
     valid, printed = None, []
     with open(os.path.join(GOLDEN, "data_next_example.txt")) as f:

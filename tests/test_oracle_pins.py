@@ -136,6 +136,37 @@ def test_symmetric_window_matches_sdpa_band_mask():
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
 
 
+def test_dense_mask_matches_sdpa_with_that_mask():
+    # an arbitrary mask: the oracle equals float64 SDPA given the same
+    # boolean matrix (rows kept non-empty so SDPA stays defined)
+    from block_sparse_masked_build_gb300 import workloads as wl
+    B, H, S, D = 1, 2, 130, 32
+    q, k, v = _qkv(B, H, S, S, D, 19)
+    dm = wl.random_dense_mask(S, S, 0.3, 32, 20)
+    dm[np.arange(S), np.arange(S)] = True
+    out, _ = oracle.softmax_attention(q, k, v, oracle.MASK_DENSE, 0, None,
+                                      None, 0.2, dense=dm)
+    np.testing.assert_allclose(out, _sdpa64(q, k, v, dm, 0.2), rtol=0,
+                               atol=1e-12)
+
+
+def test_dense_mask_special_cases():
+    # all-true dense mask changes nothing; a lower-triangular one is causal
+    B, H, S, D = 1, 1, 90, 16
+    q, k, v = _qkv(B, H, S, S, D, 21)
+    ones = np.ones((S, S), dtype=bool)
+    a, la = oracle.softmax_attention(q, k, v, oracle.MASK_DENSE, 0, None,
+                                     None, 0.3, dense=ones)
+    b, lb = oracle.softmax_attention(q, k, v, 0, 0, None, None, 0.3)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
+    c, lc = oracle.softmax_attention(q, k, v, oracle.MASK_DENSE, 0, None,
+                                     None, 0.3, dense=np.tril(ones))
+    d, ld = oracle.softmax_attention(q, k, v, MASK_CAUSAL, 0, None, None, 0.3)
+    np.testing.assert_array_equal(c, d)
+    np.testing.assert_array_equal(lc, ld)
+
+
 def test_packed_segments_match_sdpa_block_diagonal_mask():
     B, H, D = 1, 2, 32
     lens = [17, 40, 3, 60, 30]
