@@ -935,10 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<kRegsScore>();
     // one path per launch: per-element keep bits only when segment ids are
     // unsorted or an arbitrary mask is given (read once; the same for every
-    // thread)
-    if (((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0) ||
-        p.dense != nullptr)
-      score_role<D, SCORE, true, PINGPONG>(p, bars, lists, tmem);
+    // thread).  The alternating-turn instance is never launched for either.
+    if (!PINGPONG && (((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0) ||
+                      p.dense != nullptr))
+      score_role<D, SCORE, !PINGPONG, PINGPONG>(p, bars, lists, tmem);
     else
       score_role<D, SCORE, false, PINGPONG>(p, bars, lists, tmem);
   }
@@ -1005,8 +1005,10 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
   // Softmax turns alternate between the tiles only where work units are
   // long: no segment ids and at least 4096 keys.  Packed sequences and
   // short sequences give short units, where the alternation costs more
-  // than it saves.
-  const bool pp = (p.flags & BSM_MASK_SEGMENT) == 0 && p.Skv >= 4096;
+  // than it saves.  Arbitrary masks take the other instance too, which
+  // keeps the alternating one free of per-element keep bits.
+  const bool pp = (p.flags & BSM_MASK_SEGMENT) == 0 && p.Skv >= 4096 &&
+                  p.dense == nullptr;
   if (p.D == 128) {
     if (pw)
       return pp ? launch_one<128, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)

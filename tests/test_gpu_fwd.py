@@ -108,8 +108,7 @@ def test_dense_mask_elementwise(score, extra):
 
 
 def test_dense_mask_with_segments_and_long_keys_elementwise():
-    # arbitrary mask AND packed segments; 4224 keys take the kernel whose
-    # score warps alternate turns
+    # arbitrary mask AND packed segments, and alone at 4224 keys
     B, H, S, D = 1, 1, 4224, 128
     q, k, v = _qkv(B, H, H, S, S, D, seed=24)
     dm = wl.random_dense_mask(S, S, 0.5, 128, 25)
