@@ -108,40 +108,7 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
   return v;
 }
 
-// Exact element scan of a block by one warp (lanes over its columns):
-// every predicate, the arbitrary mask's bits included.  Columns past Skv
-// and rows past Sq are invisible, so a ragged block is never full.
-__device__ __forceinline__ int scan_block(const MaskInfoParams& p,
-                                          const BlockRange br, int lane,
-                                          bool seg, bool dense,
-                                          const int32_t* ks,
-                                          const int* qseg_s) {
-  bool any = false, all = !br.ragged;
-  for (int cb = 0; cb < p.bkv; cb += 32) {
-    const int k = br.c0 + cb + lane;
-    const bool kin = (cb + lane < p.bkv) && (k <= br.c1);
-    const int kv = (seg && kin) ? ks[k] : 0;
-    for (int r = br.r0; r <= br.r1; ++r) {
-      bool v = kin && base_visible(p, r, k);
-      if (seg) v = v && qseg_s[r - br.r0] == kv;
-      if (dense)
-        v = v && ((p.dense[static_cast<int64_t>(r) * p.dense_words +
-                           (k >> 5)] >>
-                   (k & 31)) &
-                  1u);
-      any |= v;
-      all &= v || (cb + lane >= p.bkv);
-    }
-    const bool wany = __any_sync(0xffffffffu, any);
-    const bool wall = __all_sync(0xffffffffu, all);
-    if (wany && !wall) break;  // already known to be partial
-  }
-  any = __any_sync(0xffffffffu, any);
-  all = __all_sync(0xffffffffu, all);
-  return any ? (all ? 2 : 1) : 0;
-}
-
-__global__ void __launch_bounds__(kMiThreads, 1)
+__global__ void __launch_bounds__(kMiThreads)
     mi_classify_kernel(const MaskInfoParams p) {
   extern __shared__ __align__(16) uint8_t dyn_s[];
   int8_t* cls_s = reinterpret_cast<int8_t*>(dyn_s);  // [nk]
@@ -216,14 +183,36 @@ __global__ void __launch_bounds__(kMiThreads, 1)
   }
   const bool ranges = seg && sorted;
 
-  const bool dense = p.dense != nullptr;
   // One warp per block (i, j).
   int my_count = 0;
   for (int j = warp; j < p.nk; j += kMiThreads / 32) {
     const BlockRange br = block_range(p, i, j);
     int c = base_class(p, br);
-    if (dense && c != 0) {
-      c = scan_block(p, br, lane, seg, dense, ks, qseg_s);
+    if (p.dense != nullptr && c != 0) {
+      // arbitrary mask: exact element scan with every predicate, the mask's
+      // bits included (columns past Skv and rows past Sq are invisible)
+      bool any = false, all = !br.ragged;
+      for (int cb = 0; cb < p.bkv; cb += 32) {
+        const int k = br.c0 + cb + lane;
+        const bool kin = (cb + lane < p.bkv) && (k <= br.c1);
+        const int kv = (seg && kin) ? ks[k] : 0;
+        for (int r = br.r0; r <= br.r1; ++r) {
+          bool v = kin && base_visible(p, r, k) &&
+                   ((p.dense[static_cast<int64_t>(r) * p.dense_words +
+                             (k >> 5)] >>
+                     (k & 31)) &
+                    1u);
+          if (seg) v = v && qseg_s[r - br.r0] == kv;
+          any |= v;
+          all &= v || (cb + lane >= p.bkv);
+        }
+        const bool wany = __any_sync(0xffffffffu, any);
+        const bool wall = __all_sync(0xffffffffu, all);
+        if (wany && !wall) break;  // already known to be partial
+      }
+      any = __any_sync(0xffffffffu, any);
+      all = __all_sync(0xffffffffu, all);
+      c = any ? (all ? 2 : 1) : 0;
     } else if (ranges && c != 0) {
       // each row sees one interval of keys: count it inside the block
       bool any = false, all = !br.ragged;
@@ -256,7 +245,25 @@ __global__ void __launch_bounds__(kMiThreads, 1)
       } else if (qmin == qmax && kmin == kmax) {
         // one segment covers the whole block: the causal/local class stands
       } else {
-        c = scan_block(p, br, lane, seg, dense, ks, qseg_s);
+        // exact element scan; columns past Skv and rows past Sq are
+        // invisible, so a ragged block is never full
+        bool any = false, all = !br.ragged;
+        for (int cb = 0; cb < p.bkv; cb += 32) {
+          const int k = br.c0 + cb + lane;
+          const bool kin = (cb + lane < p.bkv) && (k <= br.c1);
+          const int kv = kin ? ks[k] : 0;
+          for (int r = br.r0; r <= br.r1; ++r) {
+            const bool v = kin && base_visible(p, r, k) && qseg_s[r - br.r0] == kv;
+            any |= v;
+            all &= v || (cb + lane >= p.bkv);
+          }
+          const bool wany = __any_sync(0xffffffffu, any);
+          const bool wall = __all_sync(0xffffffffu, all);
+          if (wany && !wall) break;  // already known to be partial
+        }
+        any = __any_sync(0xffffffffu, any);
+        all = __all_sync(0xffffffffu, all);
+        c = any ? (all ? 2 : 1) : 0;
       }
     }
     if (lane == 0) {
@@ -445,6 +452,16 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
     return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t), stream);
   }
   cudaError_t e;
+  // All of the build's kernels ask for the largest shared-memory carveout,
+  // the one the forward runs with, so an SM need not be reconfigured
+  // between the build and the forward that follows it.
+  for (const void* k : {reinterpret_cast<const void*>(mi_classify_kernel),
+                        reinterpret_cast<const void*>(mi_scan_kernel),
+                        reinterpret_cast<const void*>(mi_compact_kernel)}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   size_t smem = static_cast<size_t>(cls_bytes(p.nk > 0 ? p.nk : 1));
   if ((p.flags & BSM_MASK_SEGMENT) && p.Skv <= kStagedKeys)
     smem += static_cast<size_t>(p.Skv) * sizeof(int32_t);
