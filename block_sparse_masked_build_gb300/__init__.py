@@ -23,5 +23,6 @@ from .api import (  # noqa: F401
     bsm_splash_fwd_workspace_bytes,
     bsm_version,
     build_mask_info,
+    pack_dense_mask,
     splash_attention,
 )

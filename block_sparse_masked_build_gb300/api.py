@@ -290,13 +290,30 @@ def build_mask_info(flags: int, B: int, Sq: int, Skv: int, block_q: int = 128,
                                dense_bits)
 
 
+def pack_dense_mask(mask: torch.Tensor) -> torch.Tensor:
+    """Bit-pack a boolean [Sq, Skv] device mask into int32 words [Sq, W],
+    W = ceil(Skv / 32): bit k % 32 of word k // 32 of row q is mask[q, k]
+    (the layout BSM_MASK_DENSE reads)."""
+    Sq, Skv = mask.shape
+    W = (Skv + 31) // 32
+    pad = torch.zeros((Sq, W * 32), dtype=torch.int64, device=mask.device)
+    pad[:, :Skv] = mask.to(torch.int64)
+    weights = torch.ones(32, dtype=torch.int64, device=mask.device)
+    weights = torch.bitwise_left_shift(weights,
+                                       torch.arange(32, device=mask.device))
+    words = (pad.view(Sq, W, 32) * weights).sum(dim=2)
+    # reinterpret the low 32 bits as int32
+    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words)
+    return words.to(torch.int32).contiguous()
+
+
 def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
                      window: int = 0, q_segment_ids=None, kv_segment_ids=None,
                      scale: float | None = None, score: int = SCORE_SOFTMAX,
                      block_q: int = 128, block_kv: int = 128,
                      mask_info: MaskInfo | None = None,
                      return_lse: bool = True, out=None, lse=None,
-                     stream=None):
+                     stream=None, dense_mask=None):
     """Block-sparse masked attention forward, q/k/v [B, H, S, D] bf16.
 
     Defaults follow hstu_ops ``pointwise_splash_attention``: scale =
@@ -305,7 +322,9 @@ def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
     the kernels run there, and ``out``/``lse`` are copied back into host
     tensors (``out``/``lse`` may be given, pinned, to be reused).
     Returns (out, lse); lse is None for the pointwise path or when
-    ``return_lse`` is False.
+    ``return_lse`` is False.  ``dense_mask`` (with MASK_DENSE) is a boolean
+    [Sq, Skv] tensor, an arbitrary mask shared by every batch row and head;
+    it is bit-packed on the device here.
     """
     B, H, Sq, D = q.shape
     Skv = k.shape[2]
@@ -327,8 +346,12 @@ def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
     else:
         qd, kd, vd, qs, ks = q, k, v, q_segment_ids, kv_segment_ids
     if mask_info is None:
+        bits = None
+        if dense_mask is not None:
+            bits = pack_dense_mask(dense_mask.to(dev))
         mask_info = build_mask_info(mask_flags, B, Sq, Skv, block_q, block_kv,
-                                    window, qs, ks, device=dev, stream=stream)
+                                    window, qs, ks, device=dev, stream=stream,
+                                    dense_bits=bits)
     od = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=dev) \
         if (host or out is None) else out
     ld = None

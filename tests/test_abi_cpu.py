@@ -181,3 +181,16 @@ def test_splash_fwd_empty_input_is_a_no_op(lib):
 def test_selftest_rejects_out_of_range_limits(lib):
     assert lib.bsm_selftest_wait_timeout(10, None) == INVALID
     assert lib.bsm_selftest_wait_timeout(10**12, None) == INVALID
+
+
+def test_torch_dense_packing_matches_layout():
+    # the binding's on-device packer (run here on CPU tensors) produces the
+    # documented layout: bit k % 32 of word k // 32 of row q
+    import numpy as np
+    import torch
+    import block_sparse_masked_build_gb300 as bsm
+    from block_sparse_masked_build_gb300 import workloads as wl
+    m = wl.random_dense_mask(45, 70, 0.5, 16, 31)
+    got = bsm.pack_dense_mask(torch.from_numpy(m)).numpy().view(np.uint32)
+    np.testing.assert_array_equal(got, wl.pack_dense_mask(m))
+    assert got.shape == (45, 3)
