@@ -222,12 +222,14 @@ def mask_name(flags, window):
                      else f"q-k<{window}")
     if flags & wl.MASK_SEGMENT:
         parts.append("same-segment")
+    if flags & wl.MASK_DENSE:
+        parts.append("arbitrary-mask")
     return "&".join(parts) or "full"
 
 
 def workload_flops(w, seg):
     return fl.unmasked_flops(w.flags, w.window, w.B, w.H, w.Sq, w.Skv_, w.D,
-                             seg, seg)
+                             dense=wl.make_dense_mask(w), q_seg=seg, kv_seg=seg)
 
 
 def config_block(w, seg, flops):
@@ -252,6 +254,9 @@ def run_ours(args, w, world, rank, local):
     flops = workload_flops(w, seg)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     segd = None if seg is None else torch.from_numpy(seg).to(dev)
+    dm = wl.make_dense_mask(w)
+    densed = (None if dm is None else
+              torch.from_numpy(wl.pack_dense_mask(dm).view(np.int32)).to(dev))
     nbytes = bsm.bsm_mask_info_bytes(w.flags, w.window, w.B, w.Sq, w.Skv_,
                                      w.block_q, w.block_kv)
     mibuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -266,7 +271,7 @@ def run_ours(args, w, world, rank, local):
             ev[0].record(stream)
         info = bsm.bsm_build_mask_info(w.flags, w.window, segd, segd, w.B,
                                        w.Sq, w.Skv_, w.block_q, w.block_kv,
-                                       mibuf, stream)
+                                       mibuf, stream, dense_bits=densed)
         if ev is not None:
             ev[1].record(stream)
         bsm.bsm_splash_fwd(qd, kd, vd, info, segd, segd, w.scale, w.score,
@@ -284,7 +289,7 @@ def run_ours(args, w, world, rank, local):
 
     info0 = bsm.bsm_build_mask_info(w.flags, w.window, segd, segd, w.B, w.Sq,
                                     w.Skv_, w.block_q, w.block_kv, mibuf,
-                                    stream)
+                                    stream, dense_bits=densed)
     mi_bytes = mask_info_bytes(w, info0)
     mi_launches = mask_info_launches(info0)
     executed_flops = executed_mma_flops(w, info0)
@@ -370,6 +375,8 @@ def mask_info_bytes(w, info):
     nnz = int(info.row_ptr[-1].item())
     seg = bool(w.flags & wl.MASK_SEGMENT)
     read = 4 * w.B * (w.Sq + w.Skv_) if seg else 0
+    if s.dense_bits:
+        read += 4 * w.Sq * s.dense_row_words
     written = (cells + 4 * cells + 4 * (T * nq + 1) + 5 * nnz
                + (8 * w.B * w.Sq + 4 if seg else 0)
                + (4 * T * s.num_super if s.super_order else 0))
@@ -442,6 +449,8 @@ def run_e2e(args, w, q, k, v, seg, flops, dev):
 
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
     sh = None if seg is None else torch.from_numpy(seg).pin_memory()
+    dm = wl.make_dense_mask(w)
+    dh = None if dm is None else torch.from_numpy(dm).pin_memory()
     oh = torch.empty((w.B, w.H, w.Sq, w.D), dtype=torch.bfloat16,
                      pin_memory=True)
     lh = (torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, pin_memory=True)
@@ -452,7 +461,8 @@ def run_e2e(args, w, q, k, v, seg, flops, dev):
         bsm.splash_attention(qh, kh, vh, mask_flags=w.flags, window=w.window,
                              q_segment_ids=sh, kv_segment_ids=sh,
                              scale=w.scale, score=w.score, block_q=w.block_q,
-                             block_kv=w.block_kv, out=oh, lse=lh)
+                             block_kv=w.block_kv, out=oh, lse=lh,
+                             dense_mask=dh)
 
     for _ in range(2):
         call()
@@ -466,7 +476,9 @@ def run_e2e(args, w, q, k, v, seg, flops, dev):
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
     ms = statistics.fmean(times)
-    h2d = qh.nbytes + kh.nbytes + vh.nbytes + (0 if sh is None else 2 * sh.nbytes)
+    h2d = (qh.nbytes + kh.nbytes + vh.nbytes
+           + (0 if sh is None else 2 * sh.nbytes)
+           + (0 if dh is None else dh.nbytes))
     d2h = oh.nbytes + (0 if lh is None else lh.nbytes)
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": args.e2e_steps,
@@ -480,18 +492,19 @@ def oracle_head(w, q, k, v, seg, b, h):
     import oracle
 
     rows = [(b, h, r) for r in range(w.Sq)]
+    dm = wl.make_dense_mask(w)
     if w.score == wl.SCORE_SOFTMAX:
         oracle.softmax_attention(q, k, v, w.flags, w.window, seg, seg,
-                                 w.scale, rows=rows)
+                                 w.scale, rows=rows, dense=dm)
     else:
         oracle.pointwise_attention(q, k, v, w.flags, w.window, seg, seg,
-                                   w.scale, rows=rows)
+                                   w.scale, rows=rows, dense=dm)
 
 
 def head_flops(w, seg, b):
     sb = None if seg is None else seg[b:b + 1]
     return fl.unmasked_flops(w.flags, w.window, 1, 1, w.Sq, w.Skv_, w.D, sb,
-                             sb)
+                             sb, dense=wl.make_dense_mask(w))
 
 
 def cpu_threads():

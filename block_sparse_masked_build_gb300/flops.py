@@ -16,6 +16,7 @@ MASK_CAUSAL = 1
 MASK_LOCAL = 2
 MASK_SEGMENT = 4
 MASK_BAND = 8
+MASK_DENSE = 16
 
 
 def _rows_range(flags, window, Sq, Skv):
@@ -31,8 +32,27 @@ def _rows_range(flags, window, Sq, Skv):
     return lo, hi
 
 
-def visible_pairs_per_row(flags, window, Sq, Skv, q_seg=None, kv_seg=None):
+def _dense_rows(flags, window, Sq, Skv, q_seg, kv_seg, dense, slab=1024):
+    """Visible keys per row with an arbitrary mask: the mask's set bits
+    inside each row's key range (and segment), counted in row slabs."""
+    lo, hi = _rows_range(flags, window, Sq, Skv)
+    dense = np.asarray(dense, dtype=bool)
+    k = np.arange(Skv)
+    out = np.zeros(Sq, dtype=np.int64)
+    for r0 in range(0, Sq, slab):
+        r = np.arange(r0, min(Sq, r0 + slab))
+        m = dense[r] & (k[None, :] >= lo[r, None]) & (k[None, :] <= hi[r, None])
+        if flags & MASK_SEGMENT:
+            m &= np.asarray(kv_seg)[None, :] == np.asarray(q_seg)[r, None]
+        out[r] = m.sum(axis=1)
+    return out
+
+
+def visible_pairs_per_row(flags, window, Sq, Skv, q_seg=None, kv_seg=None,
+                          dense=None):
     """int64 [Sq] visible keys per query row for one batch row."""
+    if flags & MASK_DENSE:
+        return _dense_rows(flags, window, Sq, Skv, q_seg, kv_seg, dense)
     lo, hi = _rows_range(flags, window, Sq, Skv)
     if not (flags & MASK_SEGMENT):
         return np.maximum(0, hi - lo + 1)
@@ -53,13 +73,18 @@ def visible_pairs_per_row(flags, window, Sq, Skv, q_seg=None, kv_seg=None):
     return out
 
 
-def visible_pairs(flags, window, B, Sq, Skv, q_seg=None, kv_seg=None):
+def visible_pairs(flags, window, B, Sq, Skv, q_seg=None, kv_seg=None,
+                  dense=None):
     """Visible pairs summed over batch rows (one head)."""
     if not (flags & MASK_SEGMENT):
-        return int(B * visible_pairs_per_row(flags, window, Sq, Skv).sum())
+        return int(B * visible_pairs_per_row(flags, window, Sq, Skv,
+                                             dense=dense).sum())
     return int(sum(visible_pairs_per_row(flags, window, Sq, Skv, q_seg[b],
-                                         kv_seg[b]).sum() for b in range(B)))
+                                         kv_seg[b], dense).sum()
+                   for b in range(B)))
 
 
-def unmasked_flops(flags, window, B, H, Sq, Skv, D, q_seg=None, kv_seg=None):
-    return 4 * D * H * visible_pairs(flags, window, B, Sq, Skv, q_seg, kv_seg)
+def unmasked_flops(flags, window, B, H, Sq, Skv, D, q_seg=None, kv_seg=None,
+                   dense=None):
+    return 4 * D * H * visible_pairs(flags, window, B, Sq, Skv, q_seg, kv_seg,
+                                     dense)

@@ -24,6 +24,7 @@ Input recipe:
 from __future__ import annotations
 
 import dataclasses
+import functools
 import math
 
 import numpy as np
@@ -58,6 +59,7 @@ class Workload:
     seg_min: int = 256
     seg_max: int = 2048
     Skv: int | None = None  # None: same as S
+    dense_p: float = 0.5    # MASK_DENSE: P(visible) inside random tiles
 
     @property
     def Sq(self) -> int:
@@ -102,6 +104,18 @@ WORKLOADS: dict[str, Workload] = {
         "cfg5_local_s32768_d128", 1, 32, 32768, 128, 128, 128,
         MASK_CAUSAL | MASK_LOCAL, 4096, SCORE_SOFTMAX, 1.0 / math.sqrt(128),
         1.0, 1005),
+    # beyond the five workloads, diagnostics of the extensions:
+    # symmetric sliding window |q - k| < 1024, B=2 H=16 S=8192 D=128
+    "next3_band_s8192_d128": Workload(
+        "next3_band_s8192_d128", 2, 16, 8192, 128, 128, 128,
+        MASK_LOCAL | MASK_BAND, 1024, SCORE_SOFTMAX, 1.0 / math.sqrt(128),
+        1.0, 1006),
+    # an arbitrary mask AND causal (128-square tiles empty, full or random
+    # with P = 0.5), B=2 H=16 S=8192 D=128
+    "next2_dense_s8192_d128": Workload(
+        "next2_dense_s8192_d128", 2, 16, 8192, 128, 128, 128,
+        MASK_DENSE | MASK_CAUSAL, 0, SCORE_SOFTMAX, 1.0 / math.sqrt(128), 1.0,
+        1007),
 }
 
 # The configuration the headline throughput is quoted on (causal, S=8192,
@@ -222,6 +236,18 @@ def pack_dense_mask(mask: np.ndarray, row_words: int = 0) -> np.ndarray:
     w = max(row_words, -(-Skv // 32))
     padded = np.zeros((Sq, w * 32), dtype=bool)
     padded[:, :Skv] = mask
-    bits = padded.reshape(Sq, w, 32).astype(np.uint64)
-    words = (bits << np.arange(32, dtype=np.uint64)).sum(axis=2)
-    return words.astype(np.uint32)
+    packed = np.packbits(padded, axis=1, bitorder="little")  # [Sq, 4w] bytes
+    return np.ascontiguousarray(packed).view("<u4").astype(np.uint32)
+
+
+@functools.lru_cache(maxsize=4)
+def _dense_cached(w: Workload) -> np.ndarray:
+    return random_dense_mask(w.Sq, w.Skv_, w.dense_p, w.block_q, w.seed + 100)
+
+
+def make_dense_mask(w: Workload) -> np.ndarray | None:
+    """The workload's boolean [Sq, Skv] arbitrary mask (MASK_DENSE), or
+    None.  The same array is returned on every call: do not modify it."""
+    if not (w.flags & MASK_DENSE):
+        return None
+    return _dense_cached(w)

@@ -230,19 +230,23 @@ def test_repeated_calls_are_deterministic():
 FULL = ["cfg1_causal_s256_d64", "cfg2_causal_s2048_d128",
         "cfg3_packed_s8192_d128", "cfg3c_causal_s8192_d128",
         "cfg4_hstu_s4096_d128", "cfg4p_hstu_s4096_d128",
-        "cfg5_local_s32768_d128"]
+        "cfg5_local_s32768_d128", "next3_band_s8192_d128",
+        "next2_dense_s8192_d128"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workloads_sampled_rows(name):
     w, q, k, v, seg = workload_inputs(name)
+    dm = wl.make_dense_mask(w)
     out, lse, _ = run_gpu(q, k, v, w.flags, w.window, seg, seg, w.scale,
-                          w.score, block_q=w.block_q, block_kv=w.block_kv)
+                          w.score, block_q=w.block_q, block_kv=w.block_kv,
+                          dense=dm)
     rows = wl.sample_rows(w, 400, seed=123, seg=seg)
     got = np.stack([out[b, h, r].numpy() for (b, h, r) in rows])
     if w.score == SM:
         ref, ref_lse = oracle.softmax_attention(q, k, v, w.flags, w.window,
-                                                seg, seg, w.scale, rows=rows)
+                                                seg, seg, w.scale, rows=rows,
+                                                dense=dm)
         compare_out(got, ref, what=name)
         compare_lse(np.array([lse[b, h, r].item() for (b, h, r) in rows]),
                     ref_lse, what=name)
@@ -250,7 +254,7 @@ def test_full_size_workloads_sampled_rows(name):
         assert torch.isfinite(out).all() and torch.isfinite(lse).all()
     else:
         ref = oracle.pointwise_attention(q, k, v, w.flags, w.window, seg, seg,
-                                         w.scale, rows=rows)
+                                         w.scale, rows=rows, dense=dm)
         compare_out(got, ref, pointwise=True, what=name)
         assert torch.isfinite(out).all()
 

@@ -69,10 +69,11 @@ def _assert_same(got, ref):
 def test_workload_mask_info_bit_exact(name):
     w = wl.WORKLOADS[name]
     seg = wl.make_segment_ids(w)
+    dm = wl.make_dense_mask(w)
     ref = oracle.mask_info(w.flags, w.window, seg, seg, w.B, w.Sq, w.Skv_,
-                           w.block_q, w.block_kv)
+                           w.block_q, w.block_kv, dense=dm)
     got = _gpu_info(w.flags, w.window, seg, seg, w.B, w.Sq, w.Skv_, w.block_q,
-                    w.block_kv)
+                    w.block_kv, dense=dm)
     _assert_same(got, ref)
     T = w.B if w.flags & 4 else 1
     _check_super_order(got, ref, T, -(-w.Sq // w.block_q), w.block_q, w.Sq)

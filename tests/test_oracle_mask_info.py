@@ -206,6 +206,26 @@ def test_dense_pack_round_trip():
     assert not words[:, 4].any() and not (words[:, 3] >> 4).any()
 
 
+def test_closed_form_flop_counts_match_oracle_counts():
+    # flops.py's per-row counting (used by the benchmark) against the
+    # oracle's element scan, for the band and arbitrary masks
+    from block_sparse_masked_build_gb300 import flops as fl
+    for flags, W in [(MASK_LOCAL | MASK_BAND, 37),
+                     (MASK_LOCAL | MASK_BAND | MASK_CAUSAL, 50)]:
+        assert fl.visible_pairs(flags, W, 1, 300, 300) == \
+            oracle.visible_pair_count(flags, W, None, None, 1, 300, 300)
+    dm = wl.random_dense_mask(300, 260, 0.4, 32, 3)
+    for flags in (oracle.MASK_DENSE, oracle.MASK_DENSE | MASK_CAUSAL):
+        assert fl.visible_pairs(flags, 0, 1, 300, 260, dense=dm) == \
+            oracle.visible_pair_count(flags, 0, None, None, 1, 300, 260,
+                                      dense=dm)
+    seg = wl.random_segment_ids(2, 300, 20, 90, 4)
+    dm = wl.random_dense_mask(300, 300, 0.5, 32, 5)
+    flags = oracle.MASK_DENSE | MASK_SEGMENT | MASK_CAUSAL
+    assert fl.visible_pairs(flags, 0, 2, 300, 300, seg, seg, dense=dm) == \
+        oracle.visible_pair_count(flags, 0, seg, seg, 2, 300, 300, dense=dm)
+
+
 def _read_golden():
     valid, printed = None, []
     with open(os.path.join(GOLDEN, "data_next_example.txt")) as f:
