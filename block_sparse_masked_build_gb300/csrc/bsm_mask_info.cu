@@ -188,9 +188,40 @@ __global__ void __launch_bounds__(kMiThreads)
   for (int j = warp; j < p.nk; j += kMiThreads / 32) {
     const BlockRange br = block_range(p, i, j);
     int c = base_class(p, br);
-    if (p.dense != nullptr && c != 0) {
-      // arbitrary mask: exact element scan with every predicate, the mask's
-      // bits included (columns past Skv and rows past Sq are invisible)
+    if (p.dense != nullptr && c != 0 && (!seg || ranges)) {
+      // arbitrary mask, every other predicate a key interval per row: count
+      // the row's mask bits inside its interval, a word at a time
+      bool any = false, all = !br.ragged;
+      for (int q = br.r0 + lane; q <= br.r1; q += 32) {
+        int lo = br.c0, hi = br.c1;
+        if (ranges) {
+          lo = max(lo, sr_s[q - br.r0].x);
+          hi = min(hi, sr_s[q - br.r0].y);
+        }
+        if (p.flags & BSM_MASK_CAUSAL) hi = min(hi, q);
+        if (p.flags & BSM_MASK_LOCAL) lo = max(lo, q - p.window + 1);
+        if (p.flags & BSM_MASK_BAND) hi = min(hi, q + p.window - 1);
+        int n = 0;
+        if (hi >= lo) {
+          const uint32_t* row = p.dense + static_cast<int64_t>(q) * p.dense_words;
+          for (int wd = lo >> 5; wd <= (hi >> 5); ++wd) {
+            const int base = wd << 5;
+            const int lb = max(lo - base, 0);        // < 32
+            const int hb = min(hi - base + 1, 32);   // >= 1
+            const uint32_t m = (hb >= 32 ? 0xffffffffu : (1u << hb) - 1u) &
+                               ~((1u << lb) - 1u);
+            n += __popc(__ldg(row + wd) & m);
+          }
+        }
+        any |= n > 0;
+        all &= n == p.bkv;
+      }
+      any = __any_sync(0xffffffffu, any);
+      all = __all_sync(0xffffffffu, all);
+      c = any ? (all ? 2 : 1) : 0;
+    } else if (p.dense != nullptr && c != 0) {
+      // arbitrary mask with unsorted segment ids: exact element scan with
+      // every predicate (columns past Skv and rows past Sq are invisible)
       bool any = false, all = !br.ragged;
       for (int cb = 0; cb < p.bkv; cb += 32) {
         const int k = br.c0 + cb + lane;

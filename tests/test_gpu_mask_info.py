@@ -158,6 +158,18 @@ def test_dense_mask_info_bit_exact(n, flags, window, bq, bkv, Sq, Skv, B):
     _assert_same(got, ref)
 
 
+@pytest.mark.parametrize("B,S,bq,bkv", [(2, 300, 32, 64), (1, 513, 64, 16)])
+def test_dense_mask_with_unsorted_segments_bit_exact(B, S, bq, bkv):
+    # arbitrary mask AND unsorted segment ids: the element-scan path
+    rng = np.random.default_rng(S)
+    seg = rng.integers(0, 3, size=(B, S)).astype(np.int32)
+    dm = wl.random_dense_mask(S, S, 0.5, 32, S + 1)
+    flags = 16 | 4 | 1
+    ref = oracle.mask_info(flags, 0, seg, seg, B, S, S, bq, bkv, dense=dm)
+    got = _gpu_info(flags, 0, seg, seg, B, S, S, bq, bkv, dense=dm)
+    _assert_same(got, ref)
+
+
 def test_super_order_absent_above_limit():
     # 9 tables x 1024 super-tiles exceed the 8192-pair table: no order, and
     # the forward falls back to taking the last super-tiles first
