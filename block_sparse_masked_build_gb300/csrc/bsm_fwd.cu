@@ -15,9 +15,9 @@
 //   warp 0      issues TMA loads: Q per query tile, K and V tiles through a
 //               ring of shared-memory slots (128-byte swizzle).
 //   warps 1,2   one MMA issuer per query tile (warp 1 also allocates the 512
-//               TMEM columns): from one lane, tcgen05 MMAs S_t = Q_t K^T (both
-//               operands in shared memory) and O_t += P_t V (P_t read from
-//               TMEM, V from shared memory).
+//               TMEM columns): the warp waits, one lane issues tcgen05 MMAs
+//               S_t = Q_t K^T (both operands in shared memory) and
+//               O_t += P_t V (P_t read from TMEM, V from shared memory).
 //   warps 4-7   score warpgroup of query tile 0, warps 8-11 of tile 1: one
 //               thread per query row (its TMEM lane).  Softmax: online
 //               max/sum with the correction of the splash notes section 15
@@ -25,13 +25,18 @@
 //               than 2^8, which leaves the final O / l exact).  Pointwise:
 //               x * sigmoid(x) / Sq with x = scale * q.k, masked -> 0
 //               (hstu_ops fwd kernel).  P goes back to TMEM as bf16 over S.
+//               In the instance used for long units without segment ids
+//               the two score warps of each SM sub-partition take their
+//               softmax turns alternately (see score_role).
 // TMEM: S0/P0 cols [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
 //
 // Element mask of a partial tile (hstu_ops `_apply_mask`): each row's visible
-// keys under causal / local masks -- and under segment ids when the kv ids are
-// sorted, via the mask-info's per-row segment ranges -- are one interval, so
-// the mask is a column-range test; unsorted segment ids are compared element
-// by element.  Key indices are the tile's true KV position.
+// keys under causal / local / band masks -- and under segment ids when the kv
+// ids are sorted, via the mask-info's per-row segment ranges -- are one
+// interval, so the mask is a column-range test; unsorted segment ids are
+// compared element by element and an arbitrary mask contributes its bits
+// (both as per-column keep bits).  Key indices are the tile's true KV
+// position.
 #include <cstdint>
 
 #include "bsm_internal.h"
