@@ -170,6 +170,16 @@ def test_splash_fwd_argument_errors(lib):
     assert _fwd(lib, info, wsb=8) == INVALID
     assert "workspace" in _lib.last_error()
     assert lib.bsm_splash_fwd_workspace_bytes() == 256 + 256 * 3 * 2048 * 2
+    # an arbitrary-mask info must carry its bits, with full rows
+    dense = _info(flags=16)
+    assert _fwd(lib, dense) == INVALID
+    assert "dense" in _lib.last_error()
+    dense.dense_bits, dense.dense_row_words = 0x80000, 7  # 256 keys: 8 words
+    assert _fwd(lib, dense) == INVALID
+    # mask info whose super-tile count does not match Sq
+    bad = _info()
+    bad.num_super = 3
+    assert _fwd(lib, bad) == INVALID
 
 
 def test_splash_fwd_empty_input_is_a_no_op(lib):
