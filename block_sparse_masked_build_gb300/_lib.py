@@ -29,6 +29,9 @@ STATUS_NAMES = {
 }
 
 
+ABI_VERSION = 200  # the struct layouts below
+
+
 class MaskSpec(ctypes.Structure):
     _fields_ = [("flags", ctypes.c_uint32), ("window", ctypes.c_int32),
                 ("dense_bits", ctypes.c_void_p),
@@ -119,7 +122,13 @@ def lib():
                     f"{LIB_PATH} is not built: run "
                     "`python -m block_sparse_masked_build_gb300.build` "
                     "(there is no CPU fallback)")
-            _lib = _declare(ctypes.CDLL(LIB_PATH))
+            loaded = _declare(ctypes.CDLL(LIB_PATH))
+            version = loaded.bsm_version()
+            if version != ABI_VERSION:
+                raise RuntimeError(
+                    f"{LIB_PATH} has ABI version {version}, this binding "
+                    f"expects {ABI_VERSION}: rebuild the library")
+            _lib = loaded
     return _lib
 
 

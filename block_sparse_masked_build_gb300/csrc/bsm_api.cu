@@ -511,6 +511,6 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq) {
 
 const char* bsm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t bsm_version(void) { return 100; }
+int32_t bsm_version(void) { return 200; }
 
 }  // extern "C"

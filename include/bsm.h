@@ -259,7 +259,9 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq);
 /* Thread-local text of the last error of this thread ("" if none). */
 const char* bsm_last_error(void);
 
-/* ABI version (major*10000 + minor*100 + patch). */
+/* ABI version (major*10000 + minor*100 + patch): 200 = 0.2.0, the
+ * mask spec and mask info with the band, arbitrary-mask and unit-order
+ * fields above. */
 int32_t bsm_version(void);
 
 #ifdef __cplusplus

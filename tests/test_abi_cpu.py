@@ -41,7 +41,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.bsm_version() == 100
+    assert lib.bsm_version() == 200 == _lib.ABI_VERSION
 
 
 def test_library_is_built_for_sm_103a(lib):
