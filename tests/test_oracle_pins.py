@@ -301,3 +301,29 @@ def test_pointwise_uses_query_length_not_key_length():
     o1 = oracle.pointwise_attention(q, k, v, 0, 0, None, None, 0.3)
     o2 = oracle.pointwise_attention(q, k2, v2, 0, 0, None, None, 0.3)
     np.testing.assert_allclose(o2, 2 * o1, rtol=1e-13, atol=1e-15)
+
+
+def test_pointwise_under_band_and_dense_masks():
+    # the pointwise path under the extra masks: an all-true arbitrary mask
+    # is the full mask, a lower-triangular one is causal, and the symmetric
+    # window equals the same band given as an arbitrary mask
+    B, H, S, D = 1, 2, 80, 16
+    q, k, v = _qkv(B, H, S, S, D, 27, sigma=0.5)
+    ones = np.ones((S, S), dtype=bool)
+    dn = oracle.MASK_DENSE
+    a = oracle.pointwise_attention(q, k, v, dn, 0, None, None, 0.3,
+                                   dense=ones)
+    np.testing.assert_array_equal(
+        a, oracle.pointwise_attention(q, k, v, 0, 0, None, None, 0.3))
+    c = oracle.pointwise_attention(q, k, v, dn, 0, None, None, 0.3,
+                                   dense=np.tril(ones))
+    np.testing.assert_array_equal(
+        c, oracle.pointwise_attention(q, k, v, MASK_CAUSAL, 0, None, None,
+                                      0.3))
+    W = 7
+    band = np.tril(ones, W - 1) & np.triu(ones, -(W - 1))
+    e = oracle.pointwise_attention(q, k, v, MASK_LOCAL | oracle.MASK_BAND, W,
+                                   None, None, 0.3)
+    np.testing.assert_array_equal(
+        e, oracle.pointwise_attention(q, k, v, dn, 0, None, None, 0.3,
+                                      dense=band))
