@@ -33,5 +33,7 @@ from .splash_oracle import (  # noqa: F401
     softmax_attention,
     softmax_attention_online,
     pointwise_attention,
+    softmax_attention_bwd,
+    pointwise_attention_bwd,
     unmasked_flops,
 )

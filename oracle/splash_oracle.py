@@ -311,3 +311,80 @@ def pointwise_attention(q, k, v, flags, window, q_seg, kv_seg, scale,
 def _order(rows):
     """Position of each (b, h, q) in the caller's ``rows`` list."""
     return {(int(b), int(h), int(q)): n for n, (b, h, q) in enumerate(rows)}
+
+
+def _bwd_inputs(q, k, v, do):
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    if kf.shape[1] != qf.shape[1]:
+        raise ValueError("the backward oracle takes as many K/V heads as "
+                         "query heads")
+    return qf, kf, vf, dof
+
+
+def softmax_attention_bwd(q, k, v, do, flags, window, q_seg, kv_seg, scale,
+                          dense=None):
+    """Gradients (dq, dk, dv) of sum(do * out) for the softmax path.
+
+    The forward of ``softmax_attention``, differentiated as written: with
+    s = scale * q k^T over the visible keys, P = softmax(s) per row and
+    out = P v,
+      dv = P^T do,  dP = do v^T,  D_q = sum_d do[q, d] out[q, d],
+      ds = P * (dP - D_q),  dq = scale * ds k,  dk = scale * ds^T q.
+    A row that sees no key has P = 0 and adds nothing.  Shapes as the
+    forward ([B, H, S, D]); returns float64 arrays.
+    """
+    qf, kf, vf, dof = _bwd_inputs(q, k, v, do)
+    B, H, Sq, D = qf.shape
+    Skv = kf.shape[2]
+    dq, dk, dv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    for b in range(B):
+        qs = None if q_seg is None else np.asarray(q_seg)[b]
+        ks = None if kv_seg is None else np.asarray(kv_seg)[b]
+        vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, None, dense)
+        any_vis = vis.any(axis=1)
+        for h in range(H):
+            a = np.where(vis, scale * (qf[b, h] @ kf[b, h].T), -np.inf)
+            M = np.where(any_vis, a.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(a - M[:, None]), 0.0)
+            L = e.sum(axis=1)
+            P = e / np.where(any_vis, L, 1.0)[:, None]
+            out = P @ vf[b, h]
+            dv[b, h] = P.T @ dof[b, h]
+            dP = dof[b, h] @ vf[b, h].T
+            Dq = (dof[b, h] * out).sum(axis=1)
+            ds = P * (dP - Dq[:, None])
+            dq[b, h] = scale * (ds @ kf[b, h])
+            dk[b, h] = scale * (ds.T @ qf[b, h])
+    return dq, dk, dv
+
+
+def pointwise_attention_bwd(q, k, v, do, flags, window, q_seg, kv_seg, scale,
+                            dense=None):
+    """Gradients (dq, dk, dv) of sum(do * out) for the pointwise path.
+
+    hstu_ops ``_pointwise_splash_attention_bwd_kernel_impl``: with
+    x = scale * q k^T, sig = logistic(x) (0 where masked) and
+    p = x * sig / Sq,
+      dv = p^T do,  dp = (do v^T) * sig * (1 + x (1 - sig)) / Sq,
+      dq = scale * dp k,  dk = scale * dp^T q,
+    each summed over every visible key (the kernel accumulates dk and dv over
+    query blocks and dq over key blocks).  Sq is the query length.
+    """
+    qf, kf, vf, dof = _bwd_inputs(q, k, v, do)
+    B, H, Sq, D = qf.shape
+    Skv = kf.shape[2]
+    dq, dk, dv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    for b in range(B):
+        qs = None if q_seg is None else np.asarray(q_seg)[b]
+        ks = None if kv_seg is None else np.asarray(kv_seg)[b]
+        vis = visibility_matrix(flags, window, Sq, Skv, qs, ks, None, dense)
+        for h in range(H):
+            x = scale * (qf[b, h] @ kf[b, h].T)
+            sig = np.where(vis, np.exp(-np.logaddexp(0.0, -x)), 0.0)
+            p = x * sig / Sq
+            dv[b, h] = p.T @ dof[b, h]
+            dp = (dof[b, h] @ vf[b, h].T) * sig * (1.0 + x * (1.0 - sig)) / Sq
+            dq[b, h] = scale * (dp @ kf[b, h])
+            dk[b, h] = scale * (dp.T @ qf[b, h])
+    return dq, dk, dv
+
