@@ -59,3 +59,40 @@ def test_single_rank_is_identity():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.impl == "ours"
     assert a.workload == "cfg3_packed_s8192_d128"
+
+
+def test_reference_arm_json_contract():
+    # the oracle arm on CPU, on the small causal workload: one JSON line
+    # with the contract's keys and a positive throughput
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    from block_sparse_masked_build_gb300 import workloads as wl
+
+    args = bench.parse_args(["--impl", "reference", "--steps", "2",
+                             "--warmup", "1", "--workload",
+                             "cfg1_causal_s256_d64"])
+    line = bench.run_reference(args, wl.WORKLOADS[args.workload])
+    json.dumps(line)
+    for key in ("metric", "value", "unit", "impl", "steps", "warmup",
+                "ms_per_step", "higher_is_better", "config", "cpu_baseline",
+                "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "cfg1_causal_s256_d64"
+
+
+def test_flop_counts_of_every_workload_are_positive():
+    # the bench's FLOP denominators, including the band and arbitrary-mask
+    # diagnostics, from the closed-form counter
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_sparse_masked_build_gb300 import workloads as wl
+
+    for name, w in wl.WORKLOADS.items():
+        if w.S > 8192:
+            continue  # the long local-window count takes longer; pinned elsewhere
+        f = bench.workload_flops(w, wl.make_segment_ids(w))
+        assert f > 0, name
