@@ -1011,9 +1011,10 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
   // long: no segment ids and at least 4096 keys.  Packed sequences and
   // short sequences give short units, where the alternation costs more
   // than it saves.  Arbitrary masks take the other instance too, which
-  // keeps the alternating one free of per-element keep bits.
+  // keeps the alternating one free of per-element keep bits; head dim 64
+  // is built without it.
   const bool pp = (p.flags & BSM_MASK_SEGMENT) == 0 && p.Skv >= 4096 &&
-                  p.dense == nullptr;
+                  p.dense == nullptr && p.D == 128;
   if (p.D == 128) {
     if (pw)
       return pp ? launch_one<128, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)
@@ -1021,11 +1022,8 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
     return pp ? launch_one<128, BSM_SCORE_SOFTMAX, true>(p, tq, tk, tv, grid, stream)
               : launch_one<128, BSM_SCORE_SOFTMAX, false>(p, tq, tk, tv, grid, stream);
   }
-  if (p.D == 64) {
-    if (pw)
-      return pp ? launch_one<64, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)
-                : launch_one<64, BSM_SCORE_POINTWISE, false>(p, tq, tk, tv, grid, stream);
-    return pp ? launch_one<64, BSM_SCORE_SOFTMAX, true>(p, tq, tk, tv, grid, stream)
+  if (p.D == 64) {  // head dim 64 uses the instance without alternation
+    return pw ? launch_one<64, BSM_SCORE_POINTWISE, false>(p, tq, tk, tv, grid, stream)
               : launch_one<64, BSM_SCORE_SOFTMAX, false>(p, tq, tk, tv, grid, stream);
   }
   return cudaErrorInvalidValue;
