@@ -7,8 +7,15 @@
 // which the implicit device synchronisation of cudaMalloc is not acceptable.
 // bsm_splash_fwd needs a caller-provided workspace; this variant uses a
 // workspace that lives in the library itself instead: a file-scope device
-// array of bsm::kFwdWorkspaceBytes (3 MiB), held by every GPU that loads the
-// library until the process exits.
+// array of bsm::kFwdWorkspaceBytes (3 MiB).
+//
+// The array is part of this file's device code.  CUDA loads a library's
+// device code into a context lazily by default (on the first use of one of
+// its kernels or symbols), and that load is when the array's 3 MiB are
+// taken.  So the first call on a device -- which looks the array up -- may
+// take device memory and synchronise; every later call in the same context
+// takes none.  Callers that reserve all free memory make one call first.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,12 +29,42 @@ namespace {
 static __device__ __align__(256) uint8_t g_fwd_scratch[bsm::kFwdWorkspaceBytes];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_fwd_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
+// Address of g_fwd_scratch per device, valid for the CUDA context it was
+// looked up in (a cudaDeviceReset makes a new primary context with a new
+// id, and the stale address is then looked up again).
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::mutex g_mu;
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+bool driver_fns() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return g_ctx_current != nullptr && g_ctx_id != nullptr;
+}
+
+// Device address of g_fwd_scratch in the current device's context.  In host
+// code the array's name is only a host-side stand-in, so the address is
+// looked up with cudaGetSymbolAddress once per device and context, with that
+// device current, and kept.
 bsm_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -39,8 +76,24 @@ bsm_status scratch_address(void** out) {
     bsm::set_last_error("bsm_splash_fwd_noalloc: device ordinal above 63");
     return BSM_ERR_UNSUPPORTED;
   }
+  if (!driver_fns()) {
+    bsm::set_last_error(
+        "bsm_splash_fwd_noalloc: cuCtxGetCurrent/cuCtxGetId unavailable");
+    return BSM_ERR_CUDA;
+  }
+  // Id of the context bound to this thread (none yet: id 0, never cached).
+  auto context_id = [](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    *id = 0;
+    return g_ctx_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+           g_ctx_id(ctx, id) == CUDA_SUCCESS;
+  };
+  unsigned long long id = 0;
+  const bool bound = context_id(&id);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchEntry& ent = g_scratch[dev];
+  if (!bound || ent.addr == nullptr || ent.ctx_id != id) {
+    // binds the device's primary context to this thread if needed
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_fwd_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -49,9 +102,15 @@ bsm_status scratch_address(void** out) {
           "array failed");
       return BSM_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    if (!context_id(&id)) {
+      bsm::set_last_error(
+          "bsm_splash_fwd_noalloc: cannot identify the CUDA context");
+      return BSM_ERR_CUDA;
+    }
+    ent.addr = p;
+    ent.ctx_id = id;
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return BSM_OK;
 }
 

@@ -207,16 +207,25 @@ size_t bsm_splash_fwd_workspace_bytes(void);
  * Plugins handed finished buffers by a host framework, serving engines that
  * reserve all free HBM up front, and loops that cannot afford cudaMalloc's
  * implicit synchronisation can call it: it takes the same arguments as
- * bsm_splash_fwd minus the workspace and allocates nothing.  Its workspace
- * is a 3 MiB (bsm_splash_fwd_workspace_bytes()) array inside the library's
- * device image, held by every GPU that loads the library until the process
- * exits.  Limits: Sq, Skv <= 262144 (else BSM_ERR_UNSUPPORTED), at most 256
- * CTAs (every supported GPU).  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture.  Every call on a device
- * shares the array: the work-unit counter in it is zeroed on `stream` before
- * each launch, and calls that overlap on the GPU (e.g. on two streams) race
- * on it and must not be issued. */
+ * bsm_splash_fwd minus the workspace and allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).  Its workspace is a 3 MiB
+ * (bsm_splash_fwd_workspace_bytes()) array in the library's own device
+ * code, held on a device from the moment that code is loaded there until
+ * the process exits.
+ * Limits: Sq, Skv <= 262144 (else BSM_ERR_UNSUPPORTED), at most 256 CTAs
+ * (every supported GPU).
+ * Set-up: the first call on a device (per CUDA context) looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and keeps it for later calls in that context.  Under CUDA's default lazy
+ * module loading that first call is also where the library's device code,
+ * with the array, is loaded into the context, which takes device memory
+ * and may synchronise: make it once, before reserving the device's free
+ * memory and before any stream capture.  Later calls take no device memory.
+ * Sharing: every call on a device uses the same array.  The work-unit
+ * counter in it is zeroed on `stream` before each launch (the rest is
+ * overwritten), so a call never depends on what an earlier call left there;
+ * calls that overlap on the GPU (e.g. on two streams) race on it and must
+ * not be issued. */
 bsm_status bsm_splash_fwd_noalloc(const void* q, const void* k, const void* v,
                                   const int64_t q_strides[3],
                                   const int64_t k_strides[3],
