@@ -10,9 +10,13 @@ outside the step's events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs the same workload on its own GPU
-(independent problems, weak scaling, no data-path collective); rank 0 prints
-one JSON line with the max step time over ranks.
+Under torchrun (N > 1) the heads are partitioned over the ranks, one rank
+per GPU, with no data-path collective (the forward of one head never needs
+another head's data).  By default the job grows with N (weak scaling): the
+N-GPU problem has N*H heads, and rank r owns heads [r*H, (r+1)*H), each rank
+holding only its own heads' q/k/v.  With ``--strong`` the workload's H heads
+are split over the ranks instead (rank r owns heads [r*H/N, (r+1)*H/N)).
+Rank 0 prints one JSON line with the max step time over ranks.
 ``--impl reference`` times the fp64 CPU oracle instead (rank 0 only).
 """
 
@@ -64,6 +68,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--strong", action="store_true",
+                   help="split the workload's heads over the ranks "
+                   "(default: each rank owns a block of H heads)")
     return p.parse_args(argv)
 
 
@@ -91,6 +98,35 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def head_partition(H: int, world: int, rank: int, group: int = 1):
+    """Heads [h0, h1) of `rank` when H heads are split over `world` ranks in
+    whole groups of `group` query heads (the heads that share one K/V head),
+    as evenly as possible; the ranges of all ranks partition [0, H)."""
+    if H % group:
+        raise ValueError("H must be a multiple of the group size")
+    ng = H // group
+    g0 = rank * ng // world
+    g1 = (rank + 1) * ng // world
+    return g0 * group, g1 * group
+
+
+def rank_seed(w, rank: int) -> int:
+    """Seed of the q/k/v draw of head block `rank` in weak scaling (block 0
+    is the single-GPU workload itself)."""
+    return w.seed + 1000 * rank
+
+
+def rank_workload(w, world: int, rank: int, strong: bool):
+    """(workload of this rank's share, h0, h1, global H).  Weak: the N-GPU
+    problem has world*H heads and rank r owns [r*H, (r+1)*H), drawn with
+    its own seed.  Strong: the workload's H heads are partitioned."""
+    if strong:
+        h0, h1 = head_partition(w.H, world, rank)
+        return w.with_(H=h1 - h0), h0, h1, w.H
+    h0, h1 = head_partition(world * w.H, world, rank)
+    return w.with_(seed=rank_seed(w, rank)), h0, h1, world * w.H
 
 
 # ------------------------------------------------------------------ peaks
@@ -249,9 +285,20 @@ def run_ours(args, w, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    q, k, v = wl.make_qkv(w)
+    wfull = w
+    # this rank's heads; segment ids and any arbitrary mask are per batch
+    # row, shared by every head, so every rank uses the same ones
+    w, h0, h1, H_global = rank_workload(wfull, world, rank, args.strong)
+    if args.strong:
+        q, k, v = (t[:, h0:h1].contiguous() for t in wl.make_qkv(wfull))
+    else:
+        q, k, v = wl.make_qkv(w)
     seg = wl.make_segment_ids(w)
-    flops = workload_flops(w, seg)
+    flops = workload_flops(w, seg) if w.H > 0 else 0
+    # unmasked FLOPs of the whole N-GPU problem (every head sees the same
+    # mask, so each rank's share is proportional to its heads)
+    job_flops = (workload_flops(wfull, seg) if args.strong
+                 else world * flops)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     segd = None if seg is None else torch.from_numpy(seg).to(dev)
     dm = wl.make_dense_mask(w)
@@ -329,7 +376,7 @@ def run_ours(args, w, world, rank, local):
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     ms_step = statistics.fmean(step_ms)
     ms_step_max = reduce_max(ms_step, world, dev)
-    value = world * flops / (ms_step_max * 1e-3) / 1e12
+    value = job_flops / (ms_step_max * 1e-3) / 1e12
     fwd_mean = statistics.fmean(fwd_ms)
     peaks = load_peaks()
     achieved = flops / (fwd_mean * 1e-3) / 1e12
@@ -345,12 +392,19 @@ def run_ours(args, w, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_step_max, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "strong" if args.strong else "weak", "vs_baseline": None,
+        "dtype": "bf16",
         "data": ("synthetic: seeded bf16 normal q/k/v; segment lengths "
                  "uniform in [256, 2048] from a seeded generator"),
-        "config": dict(config_block(w, seg, flops),
-                       parallelism=(f"{world} independent replicas"
+        "config": dict(config_block(wfull, seg, job_flops),
+                       H=H_global,
+                       parallelism=(f"heads sharded over {world} GPUs (rank "
+                                    f"r owns {h1 - h0} of {H_global} heads, "
+                                    "no collective on the data path)"
                                     if world > 1 else "single GPU")),
+        "step_ms": {"mean": round(ms_step, 5), "min": round(min(step_ms), 5),
+                    "median": round(statistics.median(step_ms), 5),
+                    "max": round(max(step_ms), 5)},
         "pct_of_bf16_peak": round(100.0 * value / world / peaks["bf16_tflops"],
                                   2),
         "roofline": roof,

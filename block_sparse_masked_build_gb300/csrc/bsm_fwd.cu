@@ -374,7 +374,7 @@ __device__ __forceinline__ void load_role(const FwdParams& p,
 // counts two arrivals), and an issuer whose tile skips an entry still waits
 // for that slot to be filled before releasing it, so the two never drift
 // more than one ring cycle apart.
-template <int D>
+template <int D, int SCORE>
 __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
                                          Bars* bars, const uint16_t* lists,
                                          uint32_t tmem, const int t) {
@@ -500,6 +500,12 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
 #pragma unroll
         for (int kk = 1; kk < kTileN / 16; ++kk)
           mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
+        if (SCORE == BSM_SCORE_POINTWISE) {  // + P_lo V (P_lo at column 64)
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(o_acc, s_acc + 64 + kk * 8, b + kk * (16 * 128 / 16),
+                   idesc_o, 1u);
+        }
         mma_commit(&bars->pv_done[t]);
         trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
       }
@@ -789,8 +795,13 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked (-inf) -> 0.
         // With sigmoid(x) = (1 + tanh(x/2)) / 2 this is g + g*tanh(x/2),
         // g = x / (2 Sq): one tanh per element, the rest on paired f32.
+        // hstu_ops multiplies the f32 scores by f32 v, so p is kept to about
+        // 16 bits: p = hi + lo, both bf16 (lo = p - hi is exact in f32), hi
+        // over S's columns [0, 64), lo over [64, 128); the MMA warp adds
+        // both products into O.
 #pragma unroll
         for (int q = 0; q < kTileN / 32; ++q) {
+          uint32_t pl[16];
 #pragma unroll
           for (int c = 32 * q; c < 32 * q + 32; c += 2) {
             float h0, h1, g0, g1, p0, p1;
@@ -799,9 +810,13 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
             ffma2v(p0, p1, g0, g1, tanh_approx(h0), tanh_approx(h1), g0, g1);
             p0 = s[c] != NEG_INF ? p0 : 0.f;
             p1 = s[c + 1] != NEG_INF ? p1 : 0.f;
-            pk[(c & 31) / 2] = pack_bf16x2(p0, p1);
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            pk[(c & 31) / 2] = hi;
+            pl[(c & 31) / 2] = pack_bf16x2(p0 - __uint_as_float(hi << 16),
+                                           p1 - __uint_as_float(hi & 0xffff0000u));
           }
           tmem_st16(s_addr + q * 16, pk);
+          tmem_st16(s_addr + 64 + q * 16, pl);
         }
       }
       tmem_st_wait();
@@ -935,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (warp == 3)
       list_role(p, bars, lists);
     else
-      mma_role<D>(p, smem, bars, lists, tmem, warp - 1);
+      mma_role<D, SCORE>(p, smem, bars, lists, tmem, warp - 1);
   } else {
     setmaxnreg_inc<kRegsScore>();
     // one path per launch: per-element keep bits only when segment ids are

@@ -15,14 +15,14 @@ MEAN_ABS = 2e-3
 LSE_REL = 1e-3
 # The pointwise path's outputs are ~1e-3 (or ~1e-6 with scale = 1/S), where
 # absolute gates say nothing, so it is also gated relative to the oracle's
-# magnitude: max error <= 2e-2 * max|ref|, and mean error <= 2^-8 * mean|ref|.
-# 2^-8 is two bf16 roundings of at most 2^-9 relative each: P is rounded to
-# bf16 before the P*V product (the precision hstu_ops itself casts p to in
-# its backward, p.astype(do.dtype)) and the output is bf16.  An exact
-# computation with just those two roundings already shows ~2.3e-3 on these
-# shapes.
+# magnitude: max error <= 2e-2 * max|ref| and mean error <= 2e-3 * mean|ref|
+# (the same 2e-2 / 2e-3 figures, relative).  hstu_ops' forward multiplies
+# f32 scores by f32 v; the kernel keeps p as a bf16 pair (hi + lo, about 16
+# bits), so only the bf16 output rounding remains.  test_pointwise_rounding
+# emulates exactly these roundings from the oracle's values and finds
+# ~1.4e-3, inside the gate; a single bf16 p would give ~2.3e-3.
 PW_MAX_REL = 2e-2
-PW_MEAN_REL = 2.0 ** -8
+PW_MEAN_REL = 2e-3
 
 
 def dense_device_bits(dense, row_words=0):

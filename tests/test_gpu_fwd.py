@@ -2,8 +2,9 @@
 
 Small cases are compared on every output element; they span several
 128-row tiles and KV tiles and end in ragged tails.  The full-size workloads
-run in the launch configuration the benchmark times and are compared on a
-seeded sample of rows (row 0, the last row, block and segment boundaries).
+run in the launch configuration the benchmark times and are compared on
+every output row (one row per 128-row query tile of every head for the
+S=32768 local window).
 """
 
 import math
@@ -124,6 +125,54 @@ def test_symmetric_window_with_segments_elementwise():
     _check_full(q, k, v, L | BD | SG, 120, seg, seg, 0.1, SM)
 
 
+# head dim 64 under every per-element mask kind, and grouped K/V heads under
+# the pointwise path and segment ids ([HSTU] _apply_mask; [NOTES] section 21
+# query head h reads K/V head h // (H / H_kv)).
+SEG_CASES = [
+    # name, B, H, Hkv, S, D, flags, score, seg kind
+    ("d64_packed_causal", 2, 2, 2, 700, 64, C | SG, SM, "sorted"),
+    ("d64_packed_full", 1, 2, 2, 520, 64, SG, SM, "sorted"),
+    ("d64_unsorted", 1, 2, 2, 512, 64, C | SG, SM, "unsorted"),
+    ("d64_packed_pointwise", 2, 2, 2, 640, 64, C | SG, PW, "sorted"),
+    ("d64_unsorted_pointwise", 1, 2, 2, 384, 64, SG, PW, "unsorted"),
+    ("gqa_pointwise", 1, 4, 2, 640, 128, C, PW, None),
+    ("gqa_packed", 2, 4, 1, 900, 128, C | SG, SM, "sorted"),
+    ("gqa_packed_pointwise", 1, 6, 2, 768, 128, C | SG, PW, "sorted"),
+    ("gqa_d64_packed", 1, 4, 2, 600, 64, C | SG, SM, "sorted"),
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES, ids=[c[0] for c in SEG_CASES])
+def test_segment_and_gqa_cases_elementwise(case):
+    name, B, H, Hkv, S, D, flags, score, kind = case
+    seed = zlib.crc32(name.encode()) % 10000
+    q, k, v = _qkv(B, H, Hkv, S, S, D, seed=seed,
+                   sigma=0.5 if score == PW else 1.0)
+    seg = None
+    if kind == "sorted":
+        seg = wl.random_segment_ids(B, S, 30, 260, seed + 1)
+    elif kind == "unsorted":
+        seg = np.random.default_rng(seed + 2).integers(
+            0, 3, size=(B, S)).astype(np.int32)
+    bq = 64 if D == 64 else 128
+    _check_full(q, k, v, flags, 0, seg, seg, 1 / math.sqrt(D), score,
+                block_q=bq, block_kv=bq)
+
+
+@pytest.mark.parametrize("score", [SM, PW])
+def test_dense_mask_d64_elementwise(score):
+    # an arbitrary mask at head dim 64, alone and with packed segments
+    B, H, S, D = 2, 2, 600, 64
+    q, k, v = _qkv(B, H, H, S, S, D, seed=27,
+                   sigma=0.5 if score == PW else 1.0)
+    dm = wl.random_dense_mask(S, S, 0.4, 64, 28)
+    _check_full(q, k, v, DN | C, 0, None, None, 0.125, score, dense=dm,
+                block_q=64, block_kv=64)
+    seg = wl.random_segment_ids(B, S, 40, 300, 29)
+    _check_full(q, k, v, DN | SG, 0, seg, seg, 0.125, score, dense=dm,
+                block_q=64, block_kv=64)
+
+
 @pytest.mark.parametrize("score", [SM, PW])
 @pytest.mark.parametrize("causal", [True, False])
 def test_packed_segments_elementwise(score, causal):
@@ -227,48 +276,79 @@ def test_repeated_calls_are_deterministic():
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
-FULL = ["cfg1_causal_s256_d64", "cfg2_causal_s2048_d128",
-        "cfg3_packed_s8192_d128", "cfg3c_causal_s8192_d128",
-        "cfg4_hstu_s4096_d128", "cfg4p_hstu_s4096_d128",
-        "cfg5_local_s32768_d128", "next3_band_s8192_d128",
-        "next2_dense_s8192_d128"]
+# Full-size workloads in the benchmark's launch configuration, compared with
+# the oracle on EVERY output row (about 25 s of host time per S=8192 or
+# S=4096 workload), except the S=32768 local window, where one seeded row of
+# every 128-row query tile of every (batch, head) is compared, plus the rows
+# where the window starts to cut (4095, 4096, 4097) and the first and last.
+FULL_ALL_ROWS = ["cfg1_causal_s256_d64", "cfg2_causal_s2048_d128",
+                 "cfg3_packed_s8192_d128", "cfg3c_causal_s8192_d128",
+                 "cfg4_hstu_s4096_d128", "cfg4p_hstu_s4096_d128",
+                 "next3_band_s8192_d128", "next2_dense_s8192_d128"]
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_workloads_sampled_rows(name):
+def _full_size_run(name):
     w, q, k, v, seg = workload_inputs(name)
     dm = wl.make_dense_mask(w)
     out, lse, _ = run_gpu(q, k, v, w.flags, w.window, seg, seg, w.scale,
                           w.score, block_q=w.block_q, block_kv=w.block_kv,
                           dense=dm)
-    rows = wl.sample_rows(w, 400, seed=123, seg=seg)
-    got = np.stack([out[b, h, r].numpy() for (b, h, r) in rows])
+    return w, q, k, v, seg, dm, out, lse
+
+
+def _full_size_properties(w, dm, out, lse):
+    # at any size: outputs are finite, and lse is finite exactly on the rows
+    # that see at least one key (a row an arbitrary mask hides completely
+    # gives out = 0 and lse = -inf)
+    assert torch.isfinite(out).all()
+    if w.score != SM:
+        return
+    if dm is None:
+        assert torch.isfinite(lse).all()
+        return
+    from block_sparse_masked_build_gb300 import flops as fl
+    seen = fl.visible_pairs_per_row(w.flags, w.window, w.Sq, w.Skv_,
+                                    dense=dm) > 0
+    seen = torch.from_numpy(seen)
+    assert torch.isfinite(lse[:, :, seen]).all()
+    assert (lse[:, :, ~seen] == float("-inf")).all()
+    assert (out[:, :, ~seen] == 0).all()
+
+
+@pytest.mark.parametrize("name", FULL_ALL_ROWS)
+def test_full_size_workloads_every_row(name):
+    w, q, k, v, seg, dm, out, lse = _full_size_run(name)
+    _full_size_properties(w, dm, out, lse)
     if w.score == SM:
         ref, ref_lse = oracle.softmax_attention(q, k, v, w.flags, w.window,
-                                                seg, seg, w.scale, rows=rows,
-                                                dense=dm)
-        compare_out(got, ref, what=name)
-        compare_lse(np.array([lse[b, h, r].item() for (b, h, r) in rows]),
-                    ref_lse, what=name)
-        # property at any size: outputs are finite, and lse is finite
-        # exactly on the rows that see at least one key (a row an arbitrary
-        # mask hides completely gives out = 0 and lse = -inf)
-        assert torch.isfinite(out).all()
-        if dm is None:
-            assert torch.isfinite(lse).all()
-        else:
-            from block_sparse_masked_build_gb300 import flops as fl
-            seen = fl.visible_pairs_per_row(w.flags, w.window, w.Sq, w.Skv_,
-                                            dense=dm) > 0
-            seen = torch.from_numpy(seen)
-            assert torch.isfinite(lse[:, :, seen]).all()
-            assert (lse[:, :, ~seen] == float("-inf")).all()
-            assert (out[:, :, ~seen] == 0).all()
+                                                seg, seg, w.scale, dense=dm)
+        compare_out(out.numpy(), ref, what=name)
+        compare_lse(lse.numpy(), ref_lse, what=name)
     else:
         ref = oracle.pointwise_attention(q, k, v, w.flags, w.window, seg, seg,
-                                         w.scale, rows=rows, dense=dm)
-        compare_out(got, ref, pointwise=True, what=name)
-        assert torch.isfinite(out).all()
+                                         w.scale, dense=dm)
+        compare_out(out.numpy(), ref, pointwise=True, what=name)
+
+
+def test_full_size_local_window_every_tile():
+    name = "cfg5_local_s32768_d128"
+    w, q, k, v, seg, dm, out, lse = _full_size_run(name)
+    _full_size_properties(w, dm, out, lse)
+    rng = np.random.default_rng(321)
+    rows = set()
+    for b in range(w.B):
+        for h in range(w.H):
+            for t0 in range(0, w.Sq, 128):
+                rows.add((b, h, t0 + int(rng.integers(min(128, w.Sq - t0)))))
+            for r in (0, w.window - 1, w.window, w.window + 1, w.Sq - 1):
+                rows.add((b, h, r))
+    rows = sorted(rows)
+    got = np.stack([out[b, h, r].numpy() for (b, h, r) in rows])
+    ref, ref_lse = oracle.softmax_attention(q, k, v, w.flags, w.window, seg,
+                                            seg, w.scale, rows=rows)
+    compare_out(got, ref, what=name)
+    compare_lse(np.array([lse[b, h, r].item() for (b, h, r) in rows]),
+                ref_lse, what=name)
 
 
 def test_constant_value_rows_full_size():

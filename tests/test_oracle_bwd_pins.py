@@ -1,4 +1,4 @@
-"""Pins of the oracle's backward (the survey's next row after the forward).
+"""Pins of the oracle's backward (gradients of both score paths).
 
 The analytic gradients are checked against central finite differences of
 the forward oracle itself -- an independent route: only the forward
