@@ -58,6 +58,11 @@ constexpr uint32_t kRegsLight = 72, kRegsScore = 208;
 constexpr int kRegsNeeded = 128 * kRegsLight + 256 * kRegsScore;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kPingPongMin = 12;  // see score_role
+// K/V ring slots at head dim 128, each holding one 128 x 128 K or V tile.
+// Five (224 KB of shared memory with the two Q tiles) keep the long units'
+// loads ahead of the alternating softmax turns; three were as fast on
+// packed sequences but 9-12 % slower on long causal and local-window units.
+constexpr int kSlots128 = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRoleLoad = 1, kRoleMma = 2, kRoleScore = 3, kRoleList = 4;
 
@@ -65,7 +70,7 @@ template <int D>
 struct Cfg {
   static constexpr int kKBlocks = D / 64;            // 128-byte k-blocks
   static constexpr int kTileBytes = kTileM * D * 2;  // Q, K or V tile
-  static constexpr int kSlots = (D == 128) ? 3 : 8;
+  static constexpr int kSlots = (D == 128) ? kSlots128 : 8;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
@@ -365,6 +370,23 @@ __device__ __forceinline__ void load_role(const FwdParams& p,
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->list_free[buf]);
   }
+  // Drain: wait for the loads already issued (after an abort some may still
+  // be landing in shared memory); the last load into each barrier completes
+  // the phase of parity (loads issued into it - 1) & 1.
+  if (lane == 0) {
+    for (int s = 0; s < C::kSlots; ++s) {
+      const uint32_t n = kv_it > static_cast<uint32_t>(s)
+                             ? (kv_it - 1 - s) / C::kSlots + 1 : 0;
+      if (n > 0 && !mbar_wait_drain(&bars->kv_full[s], (n - 1) & 1,
+                                    p.timeout_ns) && ok)
+        record_timeout(kRoleLoad, 3);
+    }
+    for (int t = 0; t < 2; ++t)
+      if (q_it[t] > 0 && !mbar_wait_drain(&bars->q_full[t], (q_it[t] - 1) & 1,
+                                          p.timeout_ns) && ok)
+        record_timeout(kRoleLoad, 4);
+  }
+  __syncwarp();
 }
 
 // MMA issuer of query tile t: warp 1 (tile 0) or warp 11 (tile 1).  The
@@ -496,15 +518,23 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
         trace(p, bars, kRoleMma, kEvPReady, t, e, unit);
         tc_fence_after();
         const uint64_t b = dv0 + vslot * kTileUnits;
-        mma_ts(o_acc, s_acc, b, idesc_o, first_pv ? 0u : 1u);
-#pragma unroll
-        for (int kk = 1; kk < kTileN / 16; ++kk)
-          mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o, 1u);
-        if (SCORE == BSM_SCORE_POINTWISE) {  // + P_lo V (P_lo at column 64)
+        if (SCORE == BSM_SCORE_SOFTMAX) {
+          // P: key 16kk..16kk+15 in TMEM columns 8kk..8kk+7
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts(o_acc, s_acc + 64 + kk * 8, b + kk * (16 * 128 / 16),
-                   idesc_o, 1u);
+            mma_ts(o_acc, s_acc + kk * 8, b + kk * (16 * 128 / 16), idesc_o,
+                   (kk > 0 || !first_pv) ? 1u : 0u);
+        } else {
+          // P = hi + lo, per 64-key half h: hi in columns 64h..64h+31, lo in
+          // 64h+32..64h+63
+#pragma unroll 2
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint32_t col = (kk >> 2) * 64 + (kk & 3) * 8;
+            mma_ts(o_acc, s_acc + col, b + kk * (16 * 128 / 16), idesc_o,
+                   (kk > 0 || !first_pv) ? 1u : 0u);
+            mma_ts(o_acc, s_acc + col + 32, b + kk * (16 * 128 / 16), idesc_o,
+                   1u);
+          }
         }
         mma_commit(&bars->pv_done[t]);
         trace(p, bars, kRoleMma, kEvPVIssued, t, e, unit);
@@ -536,10 +566,11 @@ __device__ __forceinline__ void mma_role(const FwdParams& p, uint8_t* smem,
     }
     __syncwarp();
   }
-  // Drain: every MMA issued above has completed once this arrives.
+  // Drain: every MMA issued above has completed once this arrives (waited
+  // for also after an abort, before the CTA frees TMEM).
   if (leader) {
     mma_commit(&bars->mma_done[t]);
-    if (!mbar_wait(&bars->mma_done[t], 0, abort_flag, p.timeout_ns) && ok)
+    if (!mbar_wait_drain(&bars->mma_done[t], 0, p.timeout_ns) && ok)
       record_timeout(kRoleMma, 6);
   }
   __syncwarp();
@@ -796,27 +827,32 @@ __device__ __forceinline__ void score_role(const FwdParams& p, Bars* bars,
         // With sigmoid(x) = (1 + tanh(x/2)) / 2 this is g + g*tanh(x/2),
         // g = x / (2 Sq): one tanh per element, the rest on paired f32.
         // hstu_ops multiplies the f32 scores by f32 v, so p is kept to about
-        // 16 bits: p = hi + lo, both bf16 (lo = p - hi is exact in f32), hi
-        // over S's columns [0, 64), lo over [64, 128); the MMA warp adds
-        // both products into O.
+        // 16 bits: p = hi + lo, both bf16 (lo = p - hi is exact in f32).
+        // Each 64-key half's hi and lo (32 columns each) go back over that
+        // half's own 64 columns of S; the MMA warp adds both products into O.
 #pragma unroll
-        for (int q = 0; q < kTileN / 32; ++q) {
-          uint32_t pl[16];
+        for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-          for (int c = 32 * q; c < 32 * q + 32; c += 2) {
-            float h0, h1, g0, g1, p0, p1;
-            fmul2(h0, h1, s[c], s[c + 1], p.pw_half);
-            fmul2(g0, g1, s[c], s[c + 1], p.pw_g);
-            ffma2v(p0, p1, g0, g1, tanh_approx(h0), tanh_approx(h1), g0, g1);
-            p0 = s[c] != NEG_INF ? p0 : 0.f;
-            p1 = s[c + 1] != NEG_INF ? p1 : 0.f;
-            const uint32_t hi = pack_bf16x2(p0, p1);
-            pk[(c & 31) / 2] = hi;
-            pl[(c & 31) / 2] = pack_bf16x2(p0 - __uint_as_float(hi << 16),
-                                           p1 - __uint_as_float(hi & 0xffff0000u));
+          for (int q = 0; q < 2; ++q) {
+            uint32_t pl[16];
+#pragma unroll
+            for (int c = 64 * hf + 32 * q; c < 64 * hf + 32 * q + 32; c += 2) {
+              float h0, h1, g0, g1, p0, p1;
+              fmul2(h0, h1, s[c], s[c + 1], p.pw_half);
+              fmul2(g0, g1, s[c], s[c + 1], p.pw_g);
+              ffma2v(p0, p1, g0, g1, tanh_approx(h0), tanh_approx(h1), g0,
+                     g1);
+              p0 = s[c] != NEG_INF ? p0 : 0.f;
+              p1 = s[c + 1] != NEG_INF ? p1 : 0.f;
+              const uint32_t hi = pack_bf16x2(p0, p1);
+              pk[(c & 31) / 2] = hi;
+              pl[(c & 31) / 2] =
+                  pack_bf16x2(p0 - __uint_as_float(hi << 16),
+                              p1 - __uint_as_float(hi & 0xffff0000u));
+            }
+            tmem_st16(s_addr + hf * 64 + q * 16, pk);
+            tmem_st16(s_addr + hf * 64 + 32 + q * 16, pl);
           }
-          tmem_st16(s_addr + q * 16, pk);
-          tmem_st16(s_addr + 64 + q * 16, pl);
         }
       }
       tmem_st_wait();
