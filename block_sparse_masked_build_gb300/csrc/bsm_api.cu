@@ -3,6 +3,8 @@
 // kernel launches.  Allocates no device memory.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -34,7 +36,7 @@ bool is_block_size(int32_t b) {
 
 struct MiLayout {
   size_t off_bm, off_dn, off_rp, off_idx, off_cls, off_sr, off_sf, off_so,
-      total;
+      off_stage, off_ticket, total;
 };
 
 // seg_rows = B * Sq with segment ids, else 0.
@@ -65,6 +67,14 @@ MiLayout mi_layout(int64_t tables, int64_t nq, int64_t nk, int64_t seg_rows,
   L.off_so = o;
   if (pairs <= bsm::kMaxSuperOrder)
     o = align_up(o + static_cast<size_t>(pairs) * 4, 256);
+  // one-launch build: the rows' staged lists and the (epoch, count) ticket
+  L.off_stage = o;
+  L.off_ticket = o;
+  if (bsm::mask_info_fused(tables, nq, nk)) {
+    o = align_up(o + cells * 2, 256);
+    L.off_ticket = o;
+    o = align_up(o + 8, 256);
+  }
   L.total = o;
   return L;
 }
@@ -178,6 +188,21 @@ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// A new epoch for every mask-info build (40 bits, never 0), starting at a
+// value that differs between processes, so that a ticket word left in a
+// reused buffer by an earlier build never matches.
+uint64_t next_build_epoch() {
+  static std::atomic<uint64_t> counter{
+      (static_cast<uint64_t>(
+           std::chrono::steady_clock::now().time_since_epoch().count()) *
+       0x9E3779B97F4A7C15ull) ^
+      static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&counter))};
+  constexpr uint64_t kMask = (uint64_t{1} << 40) - 1;
+  uint64_t e = 0;
+  while (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) & kMask;
+  return e;
+}
+
 }  // namespace
 
 namespace bsm {
@@ -289,6 +314,10 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
   p.super_order = mi.super_order;
   p.dense = mi.dense_bits;
   p.dense_words = mi.dense_row_words;
+  p.fused = bsm::mask_info_fused(tables, nq, nk) ? 1 : 0;
+  p.staged = reinterpret_cast<uint16_t*>(base + L.off_stage);
+  p.ticket = reinterpret_cast<unsigned long long*>(base + L.off_ticket);
+  p.epoch = next_build_epoch();
   cudaError_t e =
       bsm::launch_mask_info(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mask-info launch");

@@ -44,6 +44,11 @@ struct MaskInfoParams {
   int32_t* super_order;   // [tables * n_super] or null
   const uint32_t* dense;  // DENSE: [Sq][dense_words] bit-packed, else null
   int64_t dense_words;
+  // one-launch build: staged row lists [tables * nq][nk] and the ticket word
+  int32_t fused;
+  uint16_t* staged;
+  unsigned long long* ticket;
+  unsigned long long epoch;  // 1 .. 2^40 - 1, new for every build
 };
 
 struct FwdParams {
@@ -85,6 +90,8 @@ struct FwdParams {
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream);
+// Whether a mask of these sizes is built in one launch.
+bool mask_info_fused(int64_t tables, int64_t nq, int64_t nk);
 int fwd_grid_size(const FwdParams& p, int num_sms);
 cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv,

@@ -5,8 +5,8 @@
 // next-block table (splash notes section 21: an empty step points at the
 // next nonzero block) plus per-row CSR lists of the nonzero blocks.
 //
-// Launches:
-//   1. classify: one CTA per (table, q-block row).  Causal/local blocks are
+// Two launches for masks of up to 2^20 block cells (every workload here):
+//   classify: one CTA per (table, q-block row).  Causal/local blocks are
 //      classified exactly from the range of q - k over the block.  With
 //      segment ids the CTA first stages the table's kv ids in shared memory
 //      (up to kStagedKeys of them), checks that they are non-decreasing, and
@@ -16,13 +16,20 @@
 //      interval, so a block is classified from its rows' intervals; with
 //      unsorted ids the min/max of the ids settle most blocks and the rest
 //      are scanned element by element.  Writes block_mask, data_next, the
-//      row's nonzero count, the rows' segment ranges and the table's
-//      "not sorted" bit.
-//   2. scan: one CTA turns the counts into CSR row offsets, ORs the tables'
-//      "not sorted" bits into seg_flags[0] and orders the super-tiles; for
-//      masks of up to 2^14 block cells it also writes the nonzero lists.
-//   3. compact (larger masks only): one CTA per row writes the ascending
-//      nonzero list.
+//      row's nonzero count, the rows' segment ranges, the table's "not
+//      sorted" bit and the row's nonzero list, compacted, into a staging
+//      area.  Then it takes a ticket; the CTA that finishes last turns the
+//      counts into CSR row offsets, ORs the tables' "not sorted" bits into
+//      seg_flags[0] and orders the super-tiles (finish_tables).  The ticket
+//      word is (epoch, count): each build brings a new epoch, so no reset
+//      between builds is needed and a stale word from an earlier build, or
+//      garbage, is never counted.
+//   copy: a warp per row moves the staged list to its CSR place.  Launched
+//      with programmatic stream serialization, so it is scheduled while
+//      classify runs and waits (griddepcontrol.wait) for its completion.
+// Larger masks take three launches: classify, then one CTA for the offsets
+// and the order (finish_tables), then one CTA per row writes the ascending
+// nonzero list from block_mask.
 #include <cstdint>
 
 #include "bsm_internal.h"
@@ -32,27 +39,10 @@ namespace {
 
 constexpr int kMiThreads = 256;
 constexpr int kStagedKeys = 32768;  // kv ids staged in shared memory (128 KB)
-// Masks of at most this many block cells are compacted by the scan kernel
-// itself (one launch fewer); larger ones by one CTA per row.
-constexpr int64_t kFusedCompactCells = int64_t{1} << 14;
-
-// Ascending list of the nonzero blocks of row `row`, written by one warp.
-__device__ __forceinline__ void compact_row_warp(const MaskInfoParams& p,
-                                                 int64_t row, int lane) {
-  const int8_t* bm = p.block_mask + row * p.nk;
-  int base = p.row_ptr[row];
-  for (int j0 = 0; j0 < p.nk; j0 += 32) {
-    const int j = j0 + lane;
-    const int8_t c = j < p.nk ? bm[j] : 0;
-    const unsigned m = __ballot_sync(0xffffffffu, c != 0);
-    if (c != 0) {
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      p.kv_idx[pos] = j;
-      p.kv_cls[pos] = c;
-    }
-    base += __popc(m);
-  }
-}
+// Masks of at most this many block cells (and fewer than 2^24 rows) are
+// built in one launch.
+constexpr int64_t kFusedCells = int64_t{1} << 20;
+constexpr int kTicketBits = 24;  // count bits of the (epoch, count) word
 
 __host__ __device__ constexpr int cls_bytes(int nk) { return (nk + 15) & ~15; }
 
@@ -108,6 +98,119 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
   return v;
 }
 
+// Shared scratch of finish_tables.
+struct FinishScratch {
+  int warp_sums[32];
+  int carry;
+  unsigned long long wmax;
+};
+
+// Run by one CTA (any multiple of 32 threads): inclusive scan of the row
+// counts in row_ptr[1..R] in place (row_ptr[0] = 0), giving the CSR
+// offsets; the OR of the tables' "not sorted" bits; then, if requested, the
+// order in which the forward should take its 256-row super-tiles: by
+// decreasing work (sum over the super-tile's rows of the nonzero blocks they
+// see), so that the longest units start first and the short ones fill in at
+// the end.  `keys` holds kMaxSuperOrder words of shared memory.
+__device__ void finish_tables(const MaskInfoParams& p, FinishScratch& fs,
+                              uint32_t* keys) {
+  int32_t* row_ptr = p.row_ptr;
+  const int R = p.tables * p.nq;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int nwarps = blockDim.x / 32;
+  if (threadIdx.x == 0) {
+    row_ptr[0] = 0;
+    fs.carry = 0;
+    fs.wmax = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < R; base += blockDim.x) {
+    const int idx = base + threadIdx.x;
+    int v = idx < R ? row_ptr[idx + 1] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) fs.warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int sum = lane < nwarps ? fs.warp_sums[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, sum, o);
+        if (lane >= o) sum += n;
+      }
+      fs.warp_sums[lane] = sum;
+    }
+    __syncthreads();
+    const int carry = fs.carry;
+    const int prefix = (warp > 0 ? fs.warp_sums[warp - 1] : 0) + carry;
+    if (idx < R) row_ptr[idx + 1] = v + prefix;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) fs.carry = carry + fs.warp_sums[nwarps - 1];
+    __syncthreads();
+  }
+  if (p.flags & BSM_MASK_SEGMENT) {  // any table's kv ids not sorted
+    int any = 0;
+    for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
+      any |= p.seg_flags[1 + tb];
+    any = __syncthreads_or(any);
+    if (threadIdx.x == 0) p.seg_flags[0] = any ? 1 : 0;
+  }
+  if (p.super_order == nullptr) return;
+
+  // ---- longest-first order of the (table, super-tile) pairs
+  const int pairs = p.tables * p.n_super;  // <= kMaxSuperOrder
+  auto work = [&](int pr) -> unsigned long long {
+    const int t = pr / p.n_super, st = pr % p.n_super;
+    const int r0 = st * kUnitRows, r1 = min(p.Sq, r0 + kUnitRows);
+    unsigned long long w = 0;
+    for (int i = r0 / p.bq; i <= (r1 - 1) / p.bq; ++i) {
+      const int cnt = row_ptr[t * p.nq + i + 1] - row_ptr[t * p.nq + i];
+      const int rows = min(r1, (i + 1) * p.bq) - max(r0, i * p.bq);
+      w += static_cast<unsigned long long>(cnt) * rows;
+    }
+    return w;
+  };
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x)
+    atomicMax(&fs.wmax, work(pr));
+  __syncthreads();
+  const unsigned long long wmax = fs.wmax > 0 ? fs.wmax : 1;
+  int n2 = 1;
+  while (n2 < pairs) n2 <<= 1;
+  // key: complemented 19-bit work above the complemented 13-bit index, so
+  // an ascending sort gives decreasing work and, among equals, decreasing
+  // index (later rows first, as for a causal mask)
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    uint32_t key = 0xffffffffu;
+    if (i < pairs) {
+      const unsigned long long q = work(i) * 0x7ffffull / wmax;
+      key = (static_cast<uint32_t>(0x7ffffull - q) << 13) |
+            (0x1fffu - static_cast<uint32_t>(i));
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  // bitonic sort of keys[0..n2)
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = keys[i], b = keys[l];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < pairs; i += blockDim.x)
+    p.super_order[i] = static_cast<int32_t>(0x1fffu - (keys[i] & 0x1fffu));
+}
+
 __global__ void __launch_bounds__(kMiThreads)
     mi_classify_kernel(const MaskInfoParams p) {
   extern __shared__ __align__(16) uint8_t dyn_s[];
@@ -121,6 +224,9 @@ __global__ void __launch_bounds__(kMiThreads)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
   const int r0 = i * p.bq, r1 = min(p.Sq, r0 + p.bq) - 1;
+  // the copy kernel that follows may be scheduled now: it waits for this
+  // grid's completion before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   int qmin = kPosInf, qmax = kNegInf;
   if (seg) {
@@ -310,6 +416,21 @@ __global__ void __launch_bounds__(kMiThreads)
   for (int j = threadIdx.x; j < p.nk; j += blockDim.x) bm[j] = cls_s[j];
   if (threadIdx.x == 0) p.row_ptr[row + 1] = cnt_s;
 
+  // The row's nonzero list (ascending, uint16 `j << 2 | class`), staged at
+  // row * nk for the finishing CTA, warp 1.
+  if (p.fused && warp == 1) {
+    uint16_t* st = p.staged + row * p.nk;
+    int base = 0;
+    for (int j0 = 0; j0 < p.nk; j0 += 32) {
+      const int j = j0 + lane;
+      const int c = j < p.nk ? cls_s[j] : 0;
+      const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+      if (c != 0)
+        st[base + __popc(m & ((1u << lane) - 1u))] =
+            static_cast<uint16_t>((j << 2) | c);
+      base += __popc(m);
+    }
+  }
   // Next-block table, warp 0, right to left in chunks of 32.
   if (warp == 0) {
     int32_t* dn = p.data_next + row * p.nk;
@@ -331,118 +452,61 @@ __global__ void __launch_bounds__(kMiThreads)
       if (m) carry = ch * 32 + __ffs(m) - 1;
     }
   }
+  if (!p.fused) return;
+
+  // ---- ticket: the CTA that finishes last completes the tables.  Every
+  // thread's writes are made visible device-wide before the CTA counts
+  // itself; the word holds (epoch << kTicketBits) | CTAs counted, so a word
+  // from an earlier build (another epoch) counts as zero.
+  __shared__ int last_s;
+  __shared__ FinishScratch fs;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Install this build's epoch if the word still holds another one (the
+    // first CTA to get here does; a CTA whose swap fails finds it done:
+    // within a build only this swap changes the epoch, and counting starts
+    // after it), then count with one atomic add.
+    const int total = p.nq * p.tables;
+    const unsigned long long mine = p.epoch << kTicketBits;
+    unsigned long long cur =
+        *reinterpret_cast<volatile unsigned long long*>(p.ticket);
+    if ((cur >> kTicketBits) != p.epoch) atomicCAS(p.ticket, cur, mine);
+    const unsigned long long got = atomicAdd(p.ticket, 1ull);
+    const bool ok = (got >> kTicketBits) == p.epoch;
+    last_s = (ok && static_cast<int>(got & ((1ull << kTicketBits) - 1)) ==
+                        total - 1) ? 1 : 0;
+    __threadfence();
+  }
+  __syncthreads();
+  if (!last_s) return;
+  finish_tables(p, fs, reinterpret_cast<uint32_t*>(dyn_s));
 }
 
-// One CTA: inclusive scan of the row counts in row_ptr[1..R] in place
-// (row_ptr[0] = 0), giving the CSR offsets; then, if requested, the order in
-// which the forward should take its 256-row super-tiles: by decreasing work
-// (sum over the super-tile's rows of the nonzero blocks they see), so that
-// the longest units start first and the short ones fill in at the end.
-__global__ void __launch_bounds__(1024) mi_scan_kernel(const MaskInfoParams p) {
-  __shared__ int warp_sums[32];
-  __shared__ int carry_s;
-  __shared__ unsigned long long wmax_s;
-  __shared__ uint32_t keys[kMaxSuperOrder];
-  int32_t* row_ptr = p.row_ptr;
+// Moves each row's staged nonzero list to its CSR place, a warp per row
+// (second launch of the build; it waits for the first, whose last CTA wrote
+// the offsets).
+__global__ void __launch_bounds__(kMiThreads)
+    mi_copy_kernel(const MaskInfoParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int R = p.tables * p.nq;
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  if (threadIdx.x == 0) {
-    row_ptr[0] = 0;
-    carry_s = 0;
-    wmax_s = 0;
+  const int row = blockIdx.x * (kMiThreads / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= R) return;
+  const int start = p.row_ptr[row], cnt = p.row_ptr[row + 1] - start;
+  const uint16_t* st = p.staged + static_cast<int64_t>(row) * p.nk;
+  for (int k = lane; k < cnt; k += 32) {
+    const uint32_t e = st[k];
+    p.kv_idx[start + k] = static_cast<int32_t>(e >> 2);
+    p.kv_cls[start + k] = static_cast<int8_t>(e & 3u);
   }
-  __syncthreads();
-  for (int base = 0; base < R; base += blockDim.x) {
-    const int idx = base + threadIdx.x;
-    int v = idx < R ? row_ptr[idx + 1] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_sums[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      int s = warp_sums[lane];
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += n;
-      }
-      warp_sums[lane] = s;
-    }
-    __syncthreads();
-    const int carry = carry_s;
-    const int prefix = (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    if (idx < R) row_ptr[idx + 1] = v + prefix;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry_s = carry + warp_sums[31];
-    __syncthreads();
-  }
-  if (static_cast<int64_t>(R) * p.nk <= kFusedCompactCells) {
-    __syncthreads();  // row_ptr complete
-    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    for (int row = warp; row < R; row += blockDim.x / 32)
-      compact_row_warp(p, row, lane);
-  }
-  if (p.flags & BSM_MASK_SEGMENT) {  // any table's kv ids not sorted
-    int any = 0;
-    for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
-      any |= p.seg_flags[1 + tb];
-    any = __syncthreads_or(any);
-    if (threadIdx.x == 0) p.seg_flags[0] = any ? 1 : 0;
-  }
-  if (p.super_order == nullptr) return;
+}
 
-  // ---- longest-first order of the (table, super-tile) pairs
-  const int pairs = p.tables * p.n_super;  // <= kMaxSuperOrder
-  auto work = [&](int pr) -> unsigned long long {
-    const int t = pr / p.n_super, st = pr % p.n_super;
-    const int r0 = st * kUnitRows, r1 = min(p.Sq, r0 + kUnitRows);
-    unsigned long long w = 0;
-    for (int i = r0 / p.bq; i <= (r1 - 1) / p.bq; ++i) {
-      const int cnt = row_ptr[t * p.nq + i + 1] - row_ptr[t * p.nq + i];
-      const int rows = min(r1, (i + 1) * p.bq) - max(r0, i * p.bq);
-      w += static_cast<unsigned long long>(cnt) * rows;
-    }
-    return w;
-  };
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x)
-    atomicMax(&wmax_s, work(pr));
-  __syncthreads();
-  const unsigned long long wmax = wmax_s > 0 ? wmax_s : 1;
-  int n2 = 1;
-  while (n2 < pairs) n2 <<= 1;
-  // key: complemented 19-bit work above the complemented 13-bit index, so
-  // an ascending sort gives decreasing work and, among equals, decreasing
-  // index (later rows first, as for a causal mask)
-  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-    uint32_t key = 0xffffffffu;
-    if (i < pairs) {
-      const unsigned long long q = work(i) * 0x7ffffull / wmax;
-      key = (static_cast<uint32_t>(0x7ffffull - q) << 13) |
-            (0x1fffu - static_cast<uint32_t>(i));
-    }
-    keys[i] = key;
-  }
-  __syncthreads();
-  // bitonic sort of keys[0..n2)
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint32_t a = keys[i], b = keys[l];
-          const bool up = (i & k) == 0;
-          if ((a > b) == up) {
-            keys[i] = b;
-            keys[l] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < pairs; i += blockDim.x)
-    p.super_order[i] = static_cast<int32_t>(0x1fffu - (keys[i] & 0x1fffu));
+// Offsets and order of a mask too large for the one-launch build.
+__global__ void __launch_bounds__(1024) mi_scan_kernel(const MaskInfoParams p) {
+  __shared__ FinishScratch fs;
+  __shared__ uint32_t keys[kMaxSuperOrder];
+  finish_tables(p, fs, keys);
 }
 
 // Ascending list of the nonzero blocks of one row.
@@ -477,6 +541,11 @@ __global__ void __launch_bounds__(kMiThreads)
 
 }  // namespace
 
+bool mask_info_fused(int64_t tables, int64_t nq, int64_t nk) {
+  return tables * nq < (int64_t{1} << kTicketBits) &&
+         tables * nq * nk <= kFusedCells;
+}
+
 cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   const int R = p.tables * p.nq;
   if (R == 0) {
@@ -488,7 +557,8 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   // between the build and the forward that follows it.
   for (const void* k : {reinterpret_cast<const void*>(mi_classify_kernel),
                         reinterpret_cast<const void*>(mi_scan_kernel),
-                        reinterpret_cast<const void*>(mi_compact_kernel)}) {
+                        reinterpret_cast<const void*>(mi_compact_kernel),
+                        reinterpret_cast<const void*>(mi_copy_kernel)}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
@@ -496,6 +566,12 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   size_t smem = static_cast<size_t>(cls_bytes(p.nk > 0 ? p.nk : 1));
   if ((p.flags & BSM_MASK_SEGMENT) && p.Skv <= kStagedKeys)
     smem += static_cast<size_t>(p.Skv) * sizeof(int32_t);
+  if (p.fused && p.super_order != nullptr) {
+    // the finishing CTA sorts the super-tile keys in the same space
+    size_t n2 = 1;
+    while (n2 < static_cast<size_t>(p.tables) * p.n_super) n2 <<= 1;
+    smem = smem > 4 * n2 ? smem : 4 * n2;
+  }
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(mi_classify_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -505,11 +581,23 @@ cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream) {
   mi_classify_kernel<<<dim3(p.nq, p.tables), kMiThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.fused) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((R + kMiThreads / 32 - 1) / (kMiThreads / 32));
+    cfg.blockDim = dim3(kMiThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mi_copy_kernel, p);
+  }
   mi_scan_kernel<<<1, 1024, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (static_cast<int64_t>(R) * p.nk > kFusedCompactCells)
-    mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);
+  mi_compact_kernel<<<dim3(p.nq, p.tables), kMiThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -68,6 +68,9 @@ def test_mask_info_bytes_layout(lib, flags, B, Sq, Skv, bq, bkv):
             + _align(4 * cells) + _align(cells) + _align(8 * seg_rows)
             + _align(4 * (1 + (T if flags & 4 else 0)))
             + (_align(4 * pairs) if pairs <= 8192 else 0))
+    if T * nq < 2 ** 24 and cells <= 2 ** 20:
+        # one-launch build: uint16 staged row lists and the ticket word
+        want += _align(2 * cells) + _align(8)
     spec = MaskSpec(flags, 4096 if flags & 2 else 0)
     assert lib.bsm_mask_info_bytes(ctypes.byref(spec), B, Sq, Skv, bq,
                                    bkv) == want
