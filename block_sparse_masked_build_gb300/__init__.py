@@ -1,4 +1,5 @@
-"""GB300-native block-sparse masked attention forward (Splash-style).
+"""GB300-native block-sparse masked attention (Splash-style): forward and
+backward.
 
 The compute runs in libbsm.so (hand-written CUDA for sm_103a) behind the C
 ABI of ``include/bsm.h``; this package is its Python binding.
@@ -19,10 +20,13 @@ from .api import (  # noqa: F401
     bsm_last_error,
     bsm_mask_info_bytes,
     bsm_selftest_wait_timeout,
+    bsm_splash_bwd,
+    bsm_splash_bwd_workspace_bytes,
     bsm_splash_fwd,
     bsm_splash_fwd_workspace_bytes,
     bsm_version,
     build_mask_info,
     pack_dense_mask,
     splash_attention,
+    splash_attention_bwd,
 )

@@ -29,7 +29,7 @@ STATUS_NAMES = {
 }
 
 
-ABI_VERSION = 200  # the struct layouts below
+ABI_VERSION = 300  # the struct layouts below
 
 
 class MaskSpec(ctypes.Structure):
@@ -65,6 +65,11 @@ class MaskInfoStruct(ctypes.Structure):
 
 I64x3 = ctypes.c_int64 * 3
 
+
+class TensorView(ctypes.Structure):
+    """bsm_tensor: device data pointer and batch/head/sequence strides."""
+    _fields_ = [("data", ctypes.c_void_p), ("strides", ctypes.c_int64 * 3)]
+
 _lock = threading.Lock()
 _lib = None
 
@@ -95,6 +100,16 @@ def _declare(lib):
         c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p]
     lib.bsm_splash_fwd_workspace_bytes.restype = c.c_size_t
     lib.bsm_splash_fwd_workspace_bytes.argtypes = []
+    lib.bsm_splash_bwd_workspace_bytes.restype = c.c_size_t
+    lib.bsm_splash_bwd_workspace_bytes.argtypes = [c.c_int32, c.c_int32,
+                                                   c.c_int32, c.c_int32]
+    tv = c.POINTER(TensorView)
+    lib.bsm_splash_bwd.restype = c.c_int
+    lib.bsm_splash_bwd.argtypes = [
+        tv, tv, tv, tv, c.c_void_p, tv, c.c_int32, c.c_int32, c.c_int32,
+        c.c_int32, c.c_int32, c.c_int32, c.POINTER(MaskInfoStruct),
+        c.c_void_p, c.c_void_p, c.c_float, c.c_int32, tv, tv, tv, c.c_void_p,
+        c.c_size_t, c.c_void_p]
     lib.bsm_device_status.restype = c.c_int
     lib.bsm_device_status.argtypes = [c.c_void_p, c.POINTER(c.c_int32)]
     lib.bsm_selftest_wait_timeout.restype = c.c_int

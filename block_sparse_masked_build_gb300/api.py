@@ -15,7 +15,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import MaskInfoStruct, MaskSpec, I64x3
+from ._lib import MaskInfoStruct, MaskSpec, I64x3, TensorView
 
 MASK_CAUSAL = 1
 MASK_LOCAL = 2
@@ -224,6 +224,41 @@ def bsm_splash_fwd_noalloc(q, k, v, mask_info: MaskInfo, q_segment_ids,
         _ptr(lse), _stream_handle(stream)))
 
 
+def _view(t):
+    """bsm_tensor of a 4-D [B, heads, S, D] CUDA tensor view (or None)."""
+    if t is None:
+        return None
+    st = _strides3(t)
+    return TensorView(t.data_ptr(), st)
+
+
+def bsm_splash_bwd_workspace_bytes(B: int, H: int, Sq: int,
+                                   score: int) -> int:
+    return int(_lib.lib().bsm_splash_bwd_workspace_bytes(B, H, Sq, score))
+
+
+def bsm_splash_bwd(q, k, v, out, lse, dout, mask_info: MaskInfo,
+                   q_segment_ids, kv_segment_ids, scale: float, score: int,
+                   dq, dk, dv, stream=None, workspace=None) -> None:
+    """Gradients of sum(dout * out): dq [B,H,Sq,D], dk/dv [B,H_kv,Skv,D]
+    (bf16, CUDA), from the forward's q, k, v and (softmax) out and lse."""
+    B, H, Sq, D = q.shape
+    H_kv, Skv = k.shape[1], k.shape[2]
+    sh = _stream_handle(stream)
+    need = bsm_splash_bwd_workspace_bytes(B, H, Sq, score)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    views = [_view(t) for t in (q, k, v, out, dout, dq, dk, dv)]
+    refs = [None if x is None else ctypes.byref(x) for x in views]
+    _check(_lib.lib().bsm_splash_bwd(
+        refs[0], refs[1], refs[2], refs[3], _ptr(lse), refs[4], B, H, H_kv,
+        Sq, Skv, D, ctypes.byref(mask_info.struct), _ptr(q_segment_ids),
+        _ptr(kv_segment_ids), float(scale), int(score), refs[5], refs[6],
+        refs[7], _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        sh))
+
+
 def bsm_device_status(stream=None) -> tuple[int, list[int]]:
     detail = (ctypes.c_int32 * 4)()
     st = _lib.lib().bsm_device_status(_stream_handle(stream), detail)
@@ -305,6 +340,40 @@ def pack_dense_mask(mask: torch.Tensor) -> torch.Tensor:
     # reinterpret the low 32 bits as int32
     words = torch.where(words >= 2 ** 31, words - 2 ** 32, words)
     return words.to(torch.int32).contiguous()
+
+
+def splash_attention_bwd(q, k, v, out, lse, dout, *,
+                         mask_flags: int = MASK_CAUSAL, window: int = 0,
+                         q_segment_ids=None, kv_segment_ids=None,
+                         scale: float | None = None,
+                         score: int = SCORE_SOFTMAX, block_q: int = 128,
+                         block_kv: int = 128,
+                         mask_info: MaskInfo | None = None, stream=None,
+                         dense_mask=None):
+    """Backward of :func:`splash_attention` on CUDA tensors: returns
+    (dq, dk, dv) for the gradient ``dout`` of the output.  ``out`` and
+    ``lse`` are the forward's (softmax path; ignored for the pointwise
+    path)."""
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if mask_info is None:
+        bits = None
+        if dense_mask is not None:
+            bits = pack_dense_mask(dense_mask.to(q.device))
+        mask_info = build_mask_info(mask_flags, B, Sq, Skv, block_q, block_kv,
+                                    window, q_segment_ids, kv_segment_ids,
+                                    device=q.device, stream=stream,
+                                    dense_bits=bits)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    sm = score == SCORE_SOFTMAX
+    bsm_splash_bwd(q, k, v, out if sm else None, lse if sm else None, dout,
+                   mask_info, q_segment_ids, kv_segment_ids, scale, score, dq,
+                   dk, dv, stream)
+    return dq, dk, dv
 
 
 def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,

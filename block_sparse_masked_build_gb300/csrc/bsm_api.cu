@@ -494,11 +494,175 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
 
 size_t bsm_splash_fwd_workspace_bytes(void) { return bsm::kFwdWorkspaceBytes; }
 
+size_t bsm_splash_bwd_workspace_bytes(int32_t B, int32_t H, int32_t Sq,
+                                      int32_t score) {
+  if (B < 0 || H < 0 || Sq < 0) return 0;
+  if (score != BSM_SCORE_SOFTMAX) return 0;
+  return align_up(static_cast<size_t>(B) * H * Sq * sizeof(float), 256);
+}
+
+bsm_status bsm_splash_bwd(const bsm_tensor* q, const bsm_tensor* k,
+                          const bsm_tensor* v, const bsm_tensor* out,
+                          const float* lse, const bsm_tensor* dout, int32_t B,
+                          int32_t H, int32_t H_kv, int32_t Sq, int32_t Skv,
+                          int32_t D, const bsm_mask_info* info,
+                          const int32_t* q_segment_ids,
+                          const int32_t* kv_segment_ids, float scale,
+                          int32_t score, const bsm_tensor* dq,
+                          const bsm_tensor* dk, const bsm_tensor* dv,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  g_last_error.clear();
+  if (B < 0 || H < 0 || H_kv < 0 || Sq < 0 || Skv < 0)
+    return fail(BSM_ERR_INVALID_ARG, "negative size");
+  if (H_kv == 0 ? H != 0 : (H % H_kv) != 0)
+    return fail(BSM_ERR_INVALID_ARG, "H must be a multiple of H_kv");
+  if (D != 64 && D != 128)
+    return fail(BSM_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (Sq > bsm::kMaxSeq || Skv > bsm::kMaxSeq)
+    return fail(BSM_ERR_UNSUPPORTED, "sequence length above 262144");
+  if (score != BSM_SCORE_SOFTMAX && score != BSM_SCORE_POINTWISE)
+    return fail(BSM_ERR_INVALID_ARG, "unknown score path");
+  if (!std::isfinite(scale)) return fail(BSM_ERR_INVALID_ARG, "scale not finite");
+  const bool sm = score == BSM_SCORE_SOFTMAX;
+  if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr ||
+      dq == nullptr || dk == nullptr || dv == nullptr || (sm && out == nullptr))
+    return fail(BSM_ERR_INVALID_ARG, "NULL tensor view");
+  if (sm && lse == nullptr)
+    return fail(BSM_ERR_INVALID_ARG,
+                "the softmax backward needs the forward's out and lse");
+  if (info == nullptr) return fail(BSM_ERR_INVALID_ARG, "mask info is NULL");
+  if (info->Sq != Sq || info->Skv != Skv)
+    return fail(BSM_ERR_INVALID_ARG,
+                "mask info was built for other sequence lengths");
+  const bool seg = (info->flags & BSM_MASK_SEGMENT) != 0;
+  if (info->num_tables != (seg ? B : 1))
+    return fail(BSM_ERR_INVALID_ARG,
+                "mask info was built for another batch size");
+  if (!is_block_size(info->block_q) || !is_block_size(info->block_kv) ||
+      info->nq != (Sq + info->block_q - 1) / info->block_q ||
+      info->nk != (Skv + info->block_kv - 1) / info->block_kv)
+    return fail(BSM_ERR_INVALID_ARG, "inconsistent mask info");
+  if (seg && (q_segment_ids == nullptr || kv_segment_ids == nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "BSM_MASK_SEGMENT needs both q and kv segment ids");
+  if (!seg && (q_segment_ids != nullptr || kv_segment_ids != nullptr))
+    return fail(BSM_ERR_INVALID_ARG,
+                "segment ids given without BSM_MASK_SEGMENT");
+  if ((info->flags & BSM_MASK_DENSE) &&
+      (info->dense_bits == nullptr ||
+       info->dense_row_words < (static_cast<int64_t>(Skv) + 31) / 32))
+    return fail(BSM_ERR_INVALID_ARG, "mask info lacks its dense mask");
+  if (static_cast<int64_t>(B) * H * Sq == 0 &&
+      static_cast<int64_t>(B) * H_kv * Skv == 0)
+    return BSM_OK;
+  const size_t ws_need = bsm_splash_bwd_workspace_bytes(B, H, Sq, score);
+  if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need ||
+                      !aligned16(workspace)))
+    return fail(BSM_ERR_INVALID_ARG,
+                "workspace must be >= bsm_splash_bwd_workspace_bytes() bytes, "
+                "16-byte aligned");
+  // every view: aligned data, positive strides that are multiples of 8
+  struct View {
+    const bsm_tensor* t;
+    int64_t heads, S;
+    const char* name;
+  };
+  const View views[] = {{q, H, Sq, "q"},       {k, H_kv, Skv, "k"},
+                        {v, H_kv, Skv, "v"},   {dout, H, Sq, "dout"},
+                        {dq, H, Sq, "dq"},     {dk, H_kv, Skv, "dk"},
+                        {dv, H_kv, Skv, "dv"}, {sm ? out : dout, H, Sq, "out"}};
+  for (const View& w : views) {
+    if (w.S == 0) continue;
+    if (w.t->data == nullptr || !aligned16(w.t->data))
+      return fail(BSM_ERR_INVALID_ARG,
+                  std::string(w.name) + " must be non-NULL and 16-byte aligned");
+    const int64_t sizes[3] = {B, w.heads, w.S};
+    for (int d = 0; d < 3; ++d)
+      if (sizes[d] > 1 && (w.t->strides[d] <= 0 || w.t->strides[d] % 8 != 0))
+        return fail(BSM_ERR_INVALID_ARG,
+                    std::string(w.name) +
+                        " strides must be positive multiples of 8");
+  }
+  int num_sms = 0;
+  bsm_status s = check_device(&num_sms);
+  if (s != BSM_OK) return s;
+  CUtensorMap tq, tk, tv, tdo;
+  std::memset(&tq, 0, sizeof(tq));
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  std::memset(&tdo, 0, sizeof(tdo));
+  if (Sq > 0) {
+    s = make_map(&tq, q->data, B, H, Sq, D, q->strides, "q");
+    if (s != BSM_OK) return s;
+    s = make_map(&tdo, dout->data, B, H, Sq, D, dout->strides, "dout");
+    if (s != BSM_OK) return s;
+  }
+  if (Skv > 0) {
+    s = make_map(&tk, k->data, B, H_kv, Skv, D, k->strides, "k");
+    if (s != BSM_OK) return s;
+    s = make_map(&tv, v->data, B, H_kv, Skv, D, v->strides, "v");
+    if (s != BSM_OK) return s;
+  }
+  bsm::BwdParams p;
+  p.B = B;
+  p.H = H;
+  p.Hkv = H_kv;
+  p.Sq = Sq;
+  p.Skv = Skv;
+  p.D = D;
+  p.flags = info->flags;
+  p.window = info->window;
+  p.block_mask = info->block_mask;
+  p.mi_nq = info->nq;
+  p.mi_nk = info->nk;
+  p.bq = info->block_q;
+  p.bkv = info->block_kv;
+  p.q_seg = q_segment_ids;
+  p.kv_seg = kv_segment_ids;
+  p.dense = (info->flags & BSM_MASK_DENSE) ? info->dense_bits : nullptr;
+  p.dense_words = info->dense_row_words;
+  p.score = score;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.inv_sq = Sq > 0 ? static_cast<float>(1.0 / static_cast<double>(Sq)) : 0.f;
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.out = sm ? static_cast<const uint16_t*>(out->data) : nullptr;
+  p.o_sb = sm ? out->strides[0] : 0;
+  p.o_sh = sm ? out->strides[1] : 0;
+  p.o_ss = sm ? out->strides[2] : 0;
+  p.dout = static_cast<const uint16_t*>(dout->data);
+  p.do_sb = dout->strides[0];
+  p.do_sh = dout->strides[1];
+  p.do_ss = dout->strides[2];
+  p.dq = static_cast<uint16_t*>(dq->data);
+  p.dq_sb = dq->strides[0];
+  p.dq_sh = dq->strides[1];
+  p.dq_ss = dq->strides[2];
+  p.dk = static_cast<uint16_t*>(dk->data);
+  p.dk_sb = dk->strides[0];
+  p.dk_sh = dk->strides[1];
+  p.dk_ss = dk->strides[2];
+  p.dv = static_cast<uint16_t*>(dv->data);
+  p.dv_sb = dv->strides[0];
+  p.dv_sh = dv->strides[1];
+  p.dv_ss = dv->strides[2];
+  p.timeout_ns = wait_timeout_ns();
+  cudaError_t e = bsm::launch_splash_bwd(p, tq, tk, tv, tdo,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "splash_bwd launch");
+  return BSM_OK;
+}
+
 bsm_status bsm_device_status(void* stream, int32_t* detail) {
   g_last_error.clear();
-  int32_t rec[4] = {0, 0, 0, 0};
+  int32_t rec[4] = {0, 0, 0, 0}, brec[4] = {0, 0, 0, 0};
   cudaError_t e = bsm::read_device_error(rec, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "device status");
+  e = bsm::read_bwd_error(brec);
+  if (e != cudaSuccess) return cuda_fail(e, "device status");
+  if (rec[0] == 0 && brec[0] != 0) std::memcpy(rec, brec, sizeof(rec));
   if (detail != nullptr) std::memcpy(detail, rec, sizeof(rec));
   if (rec[0] != 0)
     return fail(BSM_ERR_DEVICE_TIMEOUT,
@@ -540,6 +704,6 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq) {
 
 const char* bsm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t bsm_version(void) { return 200; }
+int32_t bsm_version(void) { return 300; }
 
 }  // extern "C"

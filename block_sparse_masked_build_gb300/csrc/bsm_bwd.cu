@@ -1,0 +1,623 @@
+// Block-sparse masked attention backward for sm_103a (GB300): dQ, dK, dV of
+// sum(dO * out) for both score paths, over the same mask info as the
+// forward.
+//
+// Softmax path (the forward of the splash notes section 15, differentiated):
+// with s = scale * q.k over the visible keys, P = exp(s - lse) (lse of the
+// forward), D_q = sum_d dO[q, d] * out[q, d]:
+//     dV = P^T dO,  dS = P * (dO V^T - D_q),  dQ = scale dS K,
+//     dK = scale dS^T Q.
+// Pointwise path (hstu_ops `_pointwise_splash_attention_bwd_kernel_impl`):
+// with x = scale * q.k, sig = logistic(x), p = x sig / Sq (0 where masked),
+//     dV = p^T dO,  dS = (dO V^T) sig (1 + x (1 - sig)) / Sq,
+//     dQ = scale dS K,  dK = scale dS^T Q.
+// As in hstu_ops' backward, p (and dS) are rounded to the input type (bf16)
+// for the products; accumulation is f32 in TMEM.
+//
+// Two kernels, no atomics:
+//   dK/dV: one CTA per (batch, K/V head, 128-key tile); it walks the query
+//          tiles the mask info marks nonzero for its key tile (the
+//          transposed walk of the forward's), for every query head of the
+//          K/V head's group, and accumulates dV and dK in TMEM.
+//   dQ:    one CTA per (batch, head, 128-row query tile); it walks the key
+//          tiles of its row, as the forward does, and accumulates dQ.
+// A third, small kernel computes D_q (softmax path only).
+//
+// Warp roles (192 threads): warp 0 loads with TMA (the CTA's fixed pair of
+// tiles once, then the streamed pair of every step through a two-stage
+// ring), warp 1 issues the tcgen05 MMAs (lane 0) and owns the TMEM
+// allocation, warps 2-5 do the elementwise work, one thread per TMEM lane
+// (a row of the fixed tiles).  Per step, with F0/F1 the fixed tiles and
+// T0/T1 the streamed ones (dK/dV: F = K, V and T = Q, dO; dQ: F = Q, dO and
+// T = K, V):
+//     S  = F0 T0^T   -> TMEM [0, 128)      (both operands K-major in smem)
+//     dP = F1 T1^T   -> TMEM [128, 256)
+//     elementwise: P (dK/dV only) over S's columns, dS over dP's, as bf16
+//     dK/dV: dV += P T1, dK += dS T0 (A from TMEM, B = the streamed tile
+//            read MN-major) -> TMEM [256, 256 + D), [384, 384 + D)
+//     dQ:    dQ += dS T0 -> TMEM [256, 256 + D)
+// Every mbarrier wait is bounded; a role that gives up records the error
+// (read by bsm_device_status) and every role stops.
+#include <cstdint>
+
+#include "bsm_internal.h"
+#include "bsm_ptx.cuh"
+
+namespace bsm {
+
+// Error record of the backward kernels: [0] code, [1] block, [2] role,
+// [3] phase.
+__device__ int g_bwd_error[4];
+
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr int kRoleBLoad = 11, kRoleBMma = 12, kRoleBElem = 13;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kKBlocks = D / 64;            // 128-byte k-blocks
+  static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row tile
+  static constexpr int kOffF = 0;                    // fixed F0, F1
+  static constexpr int kOffT = 2 * kTileBytes;       // ring: 2 x (T0, T1)
+  static constexpr int kOffList = kOffT + 4 * kTileBytes;
+  static constexpr int kOffBar = kOffList + kMaxKvTiles * 2;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+};
+static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
+
+struct BwdBars {
+  uint64_t f_full;
+  uint64_t t_full[2], t_empty[2];
+  uint64_t s_full, dp_full, p_ready, acc_done, mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int n_list;
+};
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
+
+__device__ __forceinline__ void record_bwd_timeout(int role, int phase) {
+  if (atomicCAS(&g_bwd_error[0], 0, 1) == 0) {
+    g_bwd_error[1] = blockIdx.x;
+    g_bwd_error[2] = role;
+    g_bwd_error[3] = phase;
+  }
+}
+
+__device__ __forceinline__ bool bwarp_wait(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag,
+                                           uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Class of (128-row query tile starting at row R0) x (key tile jt) from the
+// mask-info blocks covering it: 2 if all are full, 0 if all are empty, else
+// 1; a key tile cut by the end of the keys is never full (the same
+// combination as the forward's).
+__device__ __forceinline__ int bwd_tile_class(const BwdParams& p, int table,
+                                              int R0, int jt) {
+  if (R0 >= p.Sq) return 0;
+  const int R1 = min(p.Sq, R0 + kTileM) - 1;
+  const int C0 = jt * kTileN;
+  const int C1 = min(p.Skv, C0 + kTileN) - 1;
+  const int i0 = R0 / p.bq, i1 = R1 / p.bq;
+  const int j0 = C0 / p.bkv, j1 = C1 / p.bkv;
+  const int8_t* bm =
+      p.block_mask + static_cast<int64_t>(table) * p.mi_nq * p.mi_nk;
+  bool all_full = true, any = false;
+  for (int i = i0; i <= i1; ++i)
+    for (int j = j0; j <= j1; ++j) {
+      const int c = bm[static_cast<int64_t>(i) * p.mi_nk + j];
+      all_full = all_full && (c == 2);
+      any = any || (c != 0);
+    }
+  if (!any) return 0;
+  if (all_full && C0 + kTileN <= p.Skv) return 2;
+  return 1;
+}
+
+// Visibility of (query q, key k) under every predicate of the mask (the
+// mask-info builder applies the same ones).
+__device__ __forceinline__ bool bwd_visible(const BwdParams& p, int b, int q,
+                                            int k) {
+  bool v = q < p.Sq && k < p.Skv;
+  if (p.flags & BSM_MASK_CAUSAL) v = v && (k <= q);
+  if (p.flags & BSM_MASK_LOCAL) v = v && (q - k < p.window);
+  if (p.flags & BSM_MASK_BAND) v = v && (k - q < p.window);
+  if (v && (p.flags & BSM_MASK_SEGMENT))
+    v = p.q_seg[static_cast<int64_t>(b) * p.Sq + q] ==
+        p.kv_seg[static_cast<int64_t>(b) * p.Skv + k];
+  if (v && p.dense != nullptr)
+    v = (__ldg(p.dense + static_cast<int64_t>(q) * p.dense_words + (k >> 5)) >>
+         (k & 31)) & 1u;
+  return v;
+}
+
+// The CTA's list of nonzero tiles (uint16: tile << 2 | class), built by one
+// warp into shared memory.  DKDV: the query tiles of key tile `fixed_tile`;
+// dQ: the key tiles of query tile `fixed_tile`.
+template <bool DKDV>
+__device__ __forceinline__ int build_bwd_list(const BwdParams& p, int table,
+                                              int fixed_tile, uint16_t* list) {
+  const int lane = threadIdx.x % 32;
+  const int n_tiles = DKDV ? (p.Sq + kTileM - 1) / kTileM
+                           : (p.Skv + kTileN - 1) / kTileN;
+  int n = 0;
+  for (int base = 0; base < n_tiles; base += 32) {
+    const int x = base + lane;
+    int c = 0;
+    if (x < n_tiles)
+      c = DKDV ? bwd_tile_class(p, table, x * kTileM, fixed_tile)
+               : bwd_tile_class(p, table, fixed_tile * kTileM, x);
+    const unsigned m = __ballot_sync(0xffffffffu, c != 0);
+    if (c) list[n + __popc(m & ((1u << lane) - 1u))] =
+        static_cast<uint16_t>((x << 2) | c);
+    n += __popc(m);
+  }
+  return n;
+}
+
+template <int D, bool DKDV>
+__device__ __forceinline__ void bwd_load_role(
+    const BwdParams& p, const CUtensorMap* tq, const CUtensorMap* tk,
+    const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* smem,
+    BwdBars* bars, const uint16_t* list, int b, int hq_or_hkv, int fixed_tile,
+    int n_iter) {
+  using C = BwdCfg<D>;
+  const int lane = threadIdx.x % 32;
+  volatile int* abort_flag = &bars->abort;
+  const int G = p.H / p.Hkv;
+  const int n_list = bars->n_list;
+  const uint64_t pol_fixed = l2_policy_evict_first();
+  const uint64_t pol_stream = l2_policy_evict_last();
+  bool ok = true;
+  uint32_t issued = 0;
+  if (lane == 0) {
+    // fixed pair: dK/dV: K, V of (b, hkv, key tile); dQ: Q, dO of
+    // (b, h, query tile)
+    mbar_arrive_expect_tx(&bars->f_full, 2 * C::kTileBytes);
+    const int row0 = fixed_tile * kTileM;
+    for (int kb = 0; kb < C::kKBlocks; ++kb) {
+      tma_load_4d(DKDV ? tk : tq, &bars->f_full,
+                  smem + C::kOffF + kb * kTileM * 128, kb * 64, row0,
+                  hq_or_hkv, b, pol_fixed);
+      tma_load_4d(DKDV ? tv : tdo, &bars->f_full,
+                  smem + C::kOffF + C::kTileBytes + kb * kTileM * 128,
+                  kb * 64, row0, hq_or_hkv, b, pol_fixed);
+    }
+  }
+  for (int it = 0; ok && it < n_iter; ++it) {
+    const int s = it & 1;
+    ok = bwarp_wait(&bars->t_empty[s], ((it >> 1) & 1) ^ 1, abort_flag,
+                    p.timeout_ns);
+    if (!ok) {
+      if (lane == 0) record_bwd_timeout(kRoleBLoad, 0);
+      break;
+    }
+    if (lane == 0) {
+      const int e = it % n_list;
+      const int tile = list[e] >> 2;
+      // dK/dV: Q and dO of query head hkv * G + it / n_list; dQ: K and V
+      // of the query head's K/V head
+      const int head = DKDV ? hq_or_hkv * G + it / n_list : hq_or_hkv / G;
+      uint8_t* dst = smem + C::kOffT + s * 2 * C::kTileBytes;
+      mbar_arrive_expect_tx(&bars->t_full[s], 2 * C::kTileBytes);
+      for (int kb = 0; kb < C::kKBlocks; ++kb) {
+        tma_load_4d(DKDV ? tq : tk, &bars->t_full[s], dst + kb * kTileM * 128,
+                    kb * 64, tile * kTileM, head, b, pol_stream);
+        tma_load_4d(DKDV ? tdo : tv, &bars->t_full[s],
+                    dst + C::kTileBytes + kb * kTileM * 128, kb * 64,
+                    tile * kTileM, head, b, pol_stream);
+      }
+    }
+    ++issued;
+  }
+  __syncwarp();
+  // Drain: the loads already issued land before the CTA exits.
+  if (lane == 0) {
+    if (!mbar_wait_drain(&bars->f_full, 0, p.timeout_ns) && ok)
+      record_bwd_timeout(kRoleBLoad, 1);
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t n = issued > static_cast<uint32_t>(s)
+                             ? (issued - 1 - s) / 2 + 1 : 0;
+      if (n > 0 && !mbar_wait_drain(&bars->t_full[s], (n - 1) & 1,
+                                    p.timeout_ns) && ok)
+        record_bwd_timeout(kRoleBLoad, 2);
+    }
+  }
+  __syncwarp();
+}
+
+template <int D, bool DKDV>
+__device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
+                                             BwdBars* bars, uint32_t tmem,
+                                             int n_iter) {
+  using C = BwdCfg<D>;
+  const bool leader = (threadIdx.x % 32) == 0;
+  volatile int* abort_flag = &bars->abort;
+  constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false);
+  constexpr uint32_t idesc_acc = idesc_bf16_f32(kTileM, D, true);
+  constexpr uint32_t kTileUnits = C::kTileBytes >> 4;
+  // K-major descriptors of the fixed tiles (A) and the ring (B), and the
+  // MN-major form of the ring's tiles for the accumulating products
+  const uint64_t da = sdesc_sw128(smem_u32(smem + C::kOffF), 16, 1024);
+  const uint64_t db = sdesc_sw128(smem_u32(smem + C::kOffT), 16, 1024);
+  const uint64_t dbm =
+      sdesc_sw128(smem_u32(smem + C::kOffT), kTileN * 128, 1024);
+  const uint32_t t_s = tmem, t_dp = tmem + 128;
+  const uint32_t t_acc0 = tmem + 256, t_acc1 = tmem + 384;
+  bool ok = bwarp_wait(&bars->f_full, 0, abort_flag, p.timeout_ns);
+  if (!ok && leader) record_bwd_timeout(kRoleBMma, 0);
+  for (int it = 0; ok && it < n_iter; ++it) {
+    const int s = it & 1;
+    ok = bwarp_wait(&bars->t_full[s], (it >> 1) & 1, abort_flag, p.timeout_ns);
+    if (!ok) {
+      if (leader) record_bwd_timeout(kRoleBMma, 1);
+      break;
+    }
+    const uint64_t t0 = db + s * 2 * kTileUnits;  // T0 (K-major)
+    const uint64_t t1 = t0 + kTileUnits;          // T1
+    if (leader) {
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+        mma_ss(t_s, da + off, t0 + off, idesc_s, k > 0 ? 1u : 0u);
+      }
+      mma_commit(&bars->s_full);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+        mma_ss(t_dp, da + kTileUnits + off, t1 + off, idesc_s,
+               k > 0 ? 1u : 0u);
+      }
+      mma_commit(&bars->dp_full);
+    }
+    __syncwarp();
+    ok = bwarp_wait(&bars->p_ready, it & 1, abort_flag, p.timeout_ns);
+    if (!ok) {
+      if (leader) record_bwd_timeout(kRoleBMma, 2);
+      break;
+    }
+    if (leader) {
+      tc_fence_after();
+      const uint64_t m0 = dbm + s * 2 * kTileUnits;  // T0 read MN-major
+      const uint64_t m1 = m0 + kTileUnits;           // T1 read MN-major
+      const uint32_t first = it == 0 ? 0u : 1u;
+      // bf16 A from TMEM: rows 16kk..16kk+15 of the K dimension in columns
+      // 8kk..8kk+7
+      if (DKDV) {
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // dV += P T1
+          mma_ts(t_acc0, t_s + kk * 8, m1 + kk * (16 * 128 / 16), idesc_acc,
+                 (kk > 0 || first) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // dK += dS T0
+          mma_ts(t_acc1, t_dp + kk * 8, m0 + kk * (16 * 128 / 16), idesc_acc,
+                 (kk > 0 || first) ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // dQ += dS T0
+          mma_ts(t_acc0, t_dp + kk * 8, m0 + kk * (16 * 128 / 16), idesc_acc,
+                 (kk > 0 || first) ? 1u : 0u);
+      }
+      mma_commit(&bars->t_empty[s]);
+    }
+    __syncwarp();
+  }
+  if (leader) {
+    mma_commit(&bars->acc_done);
+    mma_commit(&bars->mma_done);
+    if (!mbar_wait_drain(&bars->mma_done, 0, p.timeout_ns) && ok)
+      record_bwd_timeout(kRoleBMma, 3);
+  }
+  __syncwarp();
+}
+
+// Elementwise warps: one thread per row of the fixed tiles (TMEM lane).
+template <int D, int SCORE, bool DKDV>
+__device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
+                                              BwdBars* bars,
+                                              const uint16_t* list,
+                                              uint32_t tmem, int b,
+                                              int hq_or_hkv, int fixed_tile,
+                                              int n_iter) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4;  // TMEM lanes this warp may access
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+  volatile int* abort_flag = &bars->abort;
+  const int G = p.H / p.Hkv;
+  const int n_list = bars->n_list;
+  const float kLog2e = 1.4426950408889634f;
+  // the thread's row: a key (dK/dV) or a query (dQ)
+  const int row = fixed_tile * kTileM + r;
+  // dQ: the row's lse (log2 units) and D_q are fixed
+  float lse2_row = 0.f, delta_row = 0.f;
+  if (!DKDV && SCORE == BSM_SCORE_SOFTMAX && row < p.Sq) {
+    const int64_t i = (static_cast<int64_t>(b) * p.H + hq_or_hkv) * p.Sq + row;
+    lse2_row = p.lse[i] * kLog2e;
+    delta_row = p.delta[i];
+  }
+  bool ok = true;
+  for (int it = 0; it < n_iter; ++it) {
+    const int e = it % n_list;
+    const int tile = list[e] >> 2, cls = list[e] & 3;
+    const int head = DKDV ? hq_or_hkv * G + it / n_list : hq_or_hkv;
+    const int col0 = tile * kTileM;  // first query (dK/dV) / key (dQ)
+    ok = bwarp_wait(&bars->s_full, it & 1, abort_flag, p.timeout_ns) &&
+         bwarp_wait(&bars->dp_full, it & 1, abort_flag, p.timeout_ns);
+    if (!ok) {
+      record_bwd_timeout(kRoleBElem, 0);
+      break;
+    }
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < kTileN / 32; ++c) {
+      uint32_t sraw[32], dpraw[32];
+      tmem_ld32(t_s + c * 32, sraw);
+      tmem_ld32(t_dp + c * 32, dpraw);
+      // per-column statistics of the 32 queries of this chunk (dK/dV)
+      float lse2_c = 0.f, delta_c = 0.f;
+      const int qc = col0 + c * 32 + lane;
+      if (DKDV && SCORE == BSM_SCORE_SOFTMAX && qc < p.Sq) {
+        const int64_t i = (static_cast<int64_t>(b) * p.H + head) * p.Sq + qc;
+        lse2_c = p.lse[i] * kLog2e;
+        delta_c = p.delta[i];
+      }
+      // visibility bits of the chunk (partial tiles only)
+      uint32_t vis = 0xffffffffu;
+      if (cls == 1) {
+        vis = 0u;
+        for (int j = 0; j < 32; ++j) {
+          const int cidx = col0 + c * 32 + j;
+          const bool v = DKDV ? bwd_visible(p, b, cidx, row)
+                              : bwd_visible(p, b, row, cidx);
+          vis |= (v ? 1u : 0u) << j;
+        }
+      }
+      tmem_ld_wait();
+      uint32_t pw[16], dsw[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float pv[2], dsv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float sv = __uint_as_float(sraw[j + u]);
+          const float dpv = __uint_as_float(dpraw[j + u]);
+          const bool v = (vis >> (j + u)) & 1u;
+          if (SCORE == BSM_SCORE_SOFTMAX) {
+            const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c, j + u)
+                                  : lse2_row;
+            const float dl = DKDV ? __shfl_sync(0xffffffffu, delta_c, j + u)
+                                  : delta_row;
+            const float pr = v ? ex2_approx(fmaf(sv, p.scale_log2, -l2)) : 0.f;
+            pv[u] = pr;
+            dsv[u] = pr * (dpv - dl);
+          } else {
+            const float x = sv * p.scale;
+            const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+            pv[u] = v ? x * sig * p.inv_sq : 0.f;
+            dsv[u] = v ? dpv * sig * fmaf(x, 1.f - sig, 1.f) * p.inv_sq : 0.f;
+          }
+        }
+        pw[j / 2] = pack_bf16x2(pv[0], pv[1]);
+        dsw[j / 2] = pack_bf16x2(dsv[0], dsv[1]);
+      }
+      // P over S's columns, dS over dP's: chunk c writes columns 16c..16c+15,
+      // which this or an earlier chunk has already read
+      if (DKDV) tmem_st16(t_s + c * 16, pw);
+      tmem_st16(t_dp + c * 16, dsw);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars->p_ready);
+  }
+  if (!ok) return;
+  // ---- results: dK/dV rows (keys) or dQ rows, bf16; dK and dQ scaled
+  const bool row_ok = DKDV ? row < p.Skv : row < p.Sq;
+  if (n_iter > 0) {
+    if (!bwarp_wait(&bars->acc_done, 0, abort_flag, p.timeout_ns)) {
+      record_bwd_timeout(kRoleBElem, 1);
+      return;
+    }
+    tc_fence_after();
+  }
+#pragma unroll 1
+  for (int a = 0; a < (DKDV ? 2 : 1); ++a) {
+    // dK/dV: a = 0 is dV (TMEM 256), a = 1 dK (TMEM 384); dQ: a = 0
+    uint16_t* dst;
+    float mul;
+    if (DKDV) {
+      dst = (a == 0 ? p.dv : p.dk) +
+            static_cast<int64_t>(b) * (a == 0 ? p.dv_sb : p.dk_sb) +
+            static_cast<int64_t>(hq_or_hkv) * (a == 0 ? p.dv_sh : p.dk_sh) +
+            static_cast<int64_t>(row) * (a == 0 ? p.dv_ss : p.dk_ss);
+      mul = a == 0 ? 1.f : p.scale;
+    } else {
+      dst = p.dq + static_cast<int64_t>(b) * p.dq_sb +
+            static_cast<int64_t>(hq_or_hkv) * p.dq_sh +
+            static_cast<int64_t>(row) * p.dq_ss;
+      mul = p.scale;
+    }
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (n_iter > 0) {
+        tmem_ld32(tmem + lane_off + 256 + a * 128 + c * 32, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      if (row_ok) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * mul,
+                             __uint_as_float(o[2 * j + 1]) * mul);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st_global_v4(dst + c * 32 + v * 8, w[4 * v], w[4 * v + 1],
+                       w[4 * v + 2], w[4 * v + 3]);
+      }
+    }
+  }
+}
+
+template <int D, int SCORE, bool DKDV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    splash_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + C::kOffList);
+  const int warp = threadIdx.x / 32;
+  // grid: (tile, head, batch); dK/dV: key tile and K/V head; dQ: query tile
+  // and query head
+  const int fixed_tile = blockIdx.x;
+  const int head = blockIdx.y;
+  const int b = blockIdx.z;
+  const int table = (p.flags & BSM_MASK_SEGMENT) ? b : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->f_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->t_full[s], 1);
+      mbar_init(&bars->t_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 0) {
+    const int n = build_bwd_list<DKDV>(p, table, fixed_tile, list);
+    if (threadIdx.x == 0) bars->n_list = n;
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int n_iter = bars->n_list * (DKDV ? p.H / p.Hkv : 1);
+
+  if (warp == 0) {
+    if (n_iter > 0)
+      bwd_load_role<D, DKDV>(p, &tm_q, &tm_k, &tm_v, &tm_do, smem, bars, list,
+                             b, head, fixed_tile, n_iter);
+  } else if (warp == 1) {
+    if (n_iter > 0) bwd_mma_role<D, DKDV>(p, smem, bars, tmem, n_iter);
+  } else {
+    bwd_elem_role<D, SCORE, DKDV>(p, bars, list, tmem, b, head, fixed_tile,
+                                  n_iter);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kBwdTmemCols);
+}
+
+// D_q = sum_d dO[q, d] * out[q, d], one warp per (batch, head, row).
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const BwdParams p) {
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x +
+                      threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+  if (gw >= rows) return;
+  const int q = static_cast<int>(gw % p.Sq);
+  const int64_t bh = gw / p.Sq;
+  const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
+  const uint16_t* o = p.out + b * p.o_sb + h * p.o_sh + q * p.o_ss;
+  const uint16_t* d = p.dout + b * p.do_sb + h * p.do_sh + q * p.do_ss;
+  float acc = 0.f;
+  for (int c = lane * 2; c < p.D; c += 64) {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o + c);
+    const uint32_t dv = *reinterpret_cast<const uint32_t*>(d + c);
+    acc = fmaf(__uint_as_float(ov << 16), __uint_as_float(dv << 16), acc);
+    acc = fmaf(__uint_as_float(ov & 0xffff0000u),
+               __uint_as_float(dv & 0xffff0000u), acc);
+  }
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) p.delta[gw] = acc;
+}
+
+template <int D, int SCORE, bool DKDV>
+cudaError_t launch_bwd_one(const BwdParams& p, const CUtensorMap& tq,
+                           const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kern = splash_bwd_kernel<D, SCORE, DKDV>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = DKDV ? dim3((p.Skv + kTileN - 1) / kTileN, p.Hkv, p.B)
+                         : dim3((p.Sq + kTileM - 1) / kTileM, p.H, p.B);
+  kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+template <int D, int SCORE>
+cudaError_t launch_bwd_d(const BwdParams& p, const CUtensorMap& tq,
+                         const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (p.Skv > 0) e = launch_bwd_one<D, SCORE, true>(p, tq, tk, tv, tdo, stream);
+  if (e != cudaSuccess) return e;
+  if (p.Sq > 0) e = launch_bwd_one<D, SCORE, false>(p, tq, tk, tv, tdo, stream);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_splash_bwd(const BwdParams& p, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, cudaStream_t stream) {
+  cudaError_t e;
+  if (p.score == BSM_SCORE_SOFTMAX) {
+    const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+    if (rows > 0) {
+      bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256,
+                         0, stream>>>(p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const bool pw = p.score == BSM_SCORE_POINTWISE;
+  if (p.D == 128)
+    return pw ? launch_bwd_d<128, BSM_SCORE_POINTWISE>(p, tq, tk, tv, tdo, stream)
+              : launch_bwd_d<128, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, tdo, stream);
+  if (p.D == 64)
+    return pw ? launch_bwd_d<64, BSM_SCORE_POINTWISE>(p, tq, tk, tv, tdo, stream)
+              : launch_bwd_d<64, BSM_SCORE_SOFTMAX>(p, tq, tk, tv, tdo, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_bwd_error(int32_t out[4]) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_bwd_error, 4 * sizeof(int32_t));
+  if (e != cudaSuccess) return e;
+  const int32_t zero[4] = {0, 0, 0, 0};
+  return cudaMemcpyToSymbol(g_bwd_error, zero, 4 * sizeof(int32_t));
+}
+
+}  // namespace bsm

@@ -88,6 +88,36 @@ struct FwdParams {
   uint32_t trace_cap;
 };
 
+struct BwdParams {
+  int32_t B, H, Hkv, Sq, Skv, D;
+  // mask
+  uint32_t flags;
+  int32_t window;
+  const int8_t* block_mask;  // [tables][mi_nq][mi_nk]
+  int32_t mi_nq, mi_nk, bq, bkv;
+  const int32_t* q_seg;   // [B][Sq] (SEGMENT only)
+  const int32_t* kv_seg;  // [B][Skv]
+  const uint32_t* dense;  // DENSE: [Sq][dense_words] bit-packed, else null
+  int64_t dense_words;
+  // scores
+  int32_t score;
+  float scale, scale_log2, inv_sq;
+  const float* lse;  // forward logsumexp [B][H][Sq] (softmax)
+  float* delta;      // workspace: D_q = sum_d dO * out, [B][H][Sq] (softmax)
+  const uint16_t* out;   // forward output (softmax), bf16
+  int64_t o_sb, o_sh, o_ss;
+  const uint16_t* dout;  // gradient of the output, bf16
+  int64_t do_sb, do_sh, do_ss;
+  // gradients, bf16
+  uint16_t* dq;
+  int64_t dq_sb, dq_sh, dq_ss;
+  uint16_t* dk;
+  int64_t dk_sb, dk_sh, dk_ss;
+  uint16_t* dv;
+  int64_t dv_sb, dv_sh, dv_ss;
+  uint64_t timeout_ns;
+};
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream);
 // Whether a mask of these sizes is built in one launch.
@@ -97,6 +127,12 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               int num_sms, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+// D_q (softmax), then the dK/dV and dQ kernels.
+cudaError_t launch_splash_bwd(const BwdParams& p, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, cudaStream_t stream);
+// Reads and clears the device error record of the backward kernels.
+cudaError_t read_bwd_error(int32_t out[4]);
 // Sets the thread-local text returned by bsm_last_error().
 void set_last_error(const char* msg);
 // Reads and clears the device error record of the forward kernel TU.

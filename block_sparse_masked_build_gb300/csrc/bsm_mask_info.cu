@@ -265,11 +265,24 @@ __global__ void __launch_bounds__(kMiThreads)
     ks = ks_g;
     if (p.Skv <= kStagedKeys) {
       int32_t* ks_s = reinterpret_cast<int32_t*>(dyn_s + cls_bytes(p.nk));
-      for (int k = threadIdx.x; k < p.Skv; k += blockDim.x) ks_s[k] = ks_g[k];
+      // 16-byte loads, unrolled so that all of a thread's loads are in
+      // flight at once (the ids of a table are read by every row's CTA)
+      int k0 = 0;
+      if ((reinterpret_cast<uintptr_t>(ks_g) & 15u) == 0) {
+        const int n4 = p.Skv / 4;
+        const int4* g4 = reinterpret_cast<const int4*>(ks_g);
+        int4* s4 = reinterpret_cast<int4*>(ks_s);
+#pragma unroll 8
+        for (int k = threadIdx.x; k < n4; k += blockDim.x) s4[k] = __ldg(g4 + k);
+        k0 = 4 * n4;
+      }
+      for (int k = k0 + threadIdx.x; k < p.Skv; k += blockDim.x)
+        ks_s[k] = ks_g[k];
       __syncthreads();
       ks = ks_s;
     }
     bool unsorted = false;
+#pragma unroll 8
     for (int k = threadIdx.x; k + 1 < p.Skv; k += blockDim.x)
       unsorted |= ks[k] > ks[k + 1];
     sorted = !__syncthreads_or(unsorted);

@@ -1,5 +1,6 @@
 /*
- * bsm.h -- block-sparse masked attention forward (Splash-style) on GB300.
+ * bsm.h -- block-sparse masked attention (Splash-style) on GB300: the
+ * forward and its backward.
  *
  * C ABI of libbsm.so.  All compute runs in hand-written CUDA kernels for
  * sm_103a; there is no CPU path.  The library allocates no device memory:
@@ -239,6 +240,56 @@ bsm_status bsm_splash_fwd_noalloc(const void* q, const void* k, const void* v,
                                   int32_t score, void* out, float* lse,
                                   void* stream);
 
+/* A bf16 tensor in device memory, logical [B][heads][S][D] with head_dim
+ * contiguous; strides are in elements for the batch, head and sequence
+ * dims (multiples of 8, positive), data 16-byte aligned.  `data` is read
+ * for inputs and written for outputs. */
+typedef struct bsm_tensor {
+  void* data;
+  int64_t strides[3];
+} bsm_tensor;
+
+/* Bytes of bsm_splash_bwd's device workspace: B*H*Sq floats (the softmax
+ * path's per-row D_q = sum_d dO * out), 0 for the pointwise path. */
+size_t bsm_splash_bwd_workspace_bytes(int32_t B, int32_t H, int32_t Sq,
+                                      int32_t score);
+
+/* Backward of bsm_splash_fwd: dQ, dK, dV of sum(dout * out) over the same
+ * mask ([HSTU] _pointwise_splash_attention_bwd_kernel_impl and its
+ * launcher, which accumulate dK/dV over query blocks and dQ over key
+ * blocks; for the softmax path the forward of [NOTES] section 15,
+ * differentiated: with P = exp(scale q.k - lse) over the visible keys and
+ * D_q = sum_d dout[q, d] out[q, d],
+ *     dV = P^T dout,  dS = P * (dout V^T - D_q),
+ *     dQ = scale dS K,  dK = scale dS^T Q;
+ * pointwise: with x = scale q.k and sig = logistic(x),
+ *     dV = (x sig / Sq)^T dout,  dS = (dout V^T) sig (1 + x (1 - sig)) / Sq,
+ *     dQ = scale dS K,  dK = scale dS^T Q).
+ * P and dS are rounded to bf16 for the products (as [HSTU]'s backward
+ * casts p to the input type); accumulation is f32.
+ *   q, k, v, info, segment ids, scale, score: as given to bsm_splash_fwd
+ *   out, lse     the forward's output and logsumexp (SOFTMAX; NULL allowed
+ *                for POINTWISE)
+ *   dout         device bf16 [B][H][Sq][D]: gradient of the output
+ *   dq           device bf16 [B][H][Sq][D], written
+ *   dk, dv       device bf16 [B][H_kv][Skv][D], written; with H_kv < H the
+ *                gradient of a K/V head sums over its group of query heads
+ *   workspace    device, >= bsm_splash_bwd_workspace_bytes(B, H, Sq, score)
+ *                bytes, 16-byte aligned (may be NULL when that is 0)
+ * Rows and keys that see nothing get zero gradients.  Returns the same
+ * argument errors as bsm_splash_fwd. */
+bsm_status bsm_splash_bwd(const bsm_tensor* q, const bsm_tensor* k,
+                          const bsm_tensor* v, const bsm_tensor* out,
+                          const float* lse, const bsm_tensor* dout, int32_t B,
+                          int32_t H, int32_t H_kv, int32_t Sq, int32_t Skv,
+                          int32_t D, const bsm_mask_info* info,
+                          const int32_t* q_segment_ids,
+                          const int32_t* kv_segment_ids, float scale,
+                          int32_t score, const bsm_tensor* dq,
+                          const bsm_tensor* dk, const bsm_tensor* dv,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* Synchronise `stream` and report whether a kernel of this library gave up
  * on a bounded wait since the last call (then BSM_ERR_DEVICE_TIMEOUT; the
  * affected outputs are undefined, the CUDA context stays usable).  If
@@ -268,9 +319,9 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq);
 /* Thread-local text of the last error of this thread ("" if none). */
 const char* bsm_last_error(void);
 
-/* ABI version (major*10000 + minor*100 + patch): 200 = 0.2.0, the
- * mask spec and mask info with the band, arbitrary-mask and unit-order
- * fields above. */
+/* ABI version (major*10000 + minor*100 + patch): 300 = 0.3.0, the
+ * backward entry points and bsm_tensor added to 0.2.0's forward, mask spec
+ * and mask info. */
 int32_t bsm_version(void);
 
 #ifdef __cplusplus

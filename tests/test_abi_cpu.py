@@ -34,6 +34,7 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("bsm_mask_info_bytes", "bsm_build_mask_info", "bsm_splash_fwd",
+              "bsm_splash_bwd", "bsm_splash_bwd_workspace_bytes",
               "bsm_device_status", "bsm_last_error", "bsm_version"):
         assert n in names
 
@@ -41,7 +42,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.bsm_version() == 200 == _lib.ABI_VERSION
+    assert lib.bsm_version() == 300 == _lib.ABI_VERSION
 
 
 def test_library_is_built_for_sm_103a(lib):
@@ -207,3 +208,12 @@ def test_torch_dense_packing_matches_layout():
     got = bsm.pack_dense_mask(torch.from_numpy(m)).numpy().view(np.uint32)
     np.testing.assert_array_equal(got, wl.pack_dense_mask(m))
     assert got.shape == (45, 3)
+
+
+def test_bwd_workspace_bytes(lib):
+    # the softmax backward keeps D_q = sum_d dO * out per row (f32), the
+    # pointwise one needs no workspace
+    assert lib.bsm_splash_bwd_workspace_bytes(2, 16, 8192, 0) == 2 * 16 * 8192 * 4
+    assert lib.bsm_splash_bwd_workspace_bytes(1, 3, 100, 0) == 1280
+    assert lib.bsm_splash_bwd_workspace_bytes(2, 16, 8192, 1) == 0
+    assert lib.bsm_splash_bwd_workspace_bytes(-1, 16, 8192, 0) == 0
