@@ -67,6 +67,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--bwd", action="store_true",
+                   help="time the backward (dQ, dK, dV) instead (diagnostic)")
     p.add_argument("--strong", action="store_true",
                    help="split the workload's heads over the ranks "
                    "(default: each rank owns a block of H heads)")
@@ -418,6 +420,83 @@ def run_ours(args, w, world, rank, local):
     return line
 
 
+def run_bwd(args, w, dev):
+    """Backward diagnostic: dQ, dK, dV of the workload (single GPU), timed
+    per launch set with CUDA events, L2 flushed between steps.  FLOPs count
+    the five products per visible (q, k) pair (q.k, dO.v, P^T dO, dS^T Q,
+    dS K): 10 * D each, 2.5 times the forward's."""
+    import block_sparse_masked_build_gb300 as bsm
+
+    q, k, v = wl.make_qkv(w)
+    g = torch.Generator().manual_seed(w.seed + 7)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    seg = wl.make_segment_ids(w)
+    fwd_flops = workload_flops(w, seg)
+    flops = fwd_flops * 10 // 4
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    segd = None if seg is None else torch.from_numpy(seg).to(dev)
+    dm = wl.make_dense_mask(w)
+    densed = (None if dm is None else
+              torch.from_numpy(wl.pack_dense_mask(dm).view(np.int32)).to(dev))
+    info = bsm.build_mask_info(w.flags, w.B, w.Sq, w.Skv_, w.block_q,
+                               w.block_kv, w.window, segd, segd, device=dev,
+                               dense_bits=densed)
+    out, lse = bsm.splash_attention(qd, kd, vd, mask_flags=w.flags,
+                                    window=w.window, q_segment_ids=segd,
+                                    kv_segment_ids=segd, scale=w.scale,
+                                    score=w.score, mask_info=info)
+    dq, dk, dv = (torch.empty_like(t) for t in (qd, kd, vd))
+    ws_n = bsm.bsm_splash_bwd_workspace_bytes(w.B, w.H, w.Sq, w.score)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sm = w.score == wl.SCORE_SOFTMAX
+
+    def step():
+        bsm.bsm_splash_bwd(qd, kd, vd, out if sm else None,
+                           lse if sm else None, dod, info, segd, segd,
+                           w.scale, w.score, dq, dk, dv, stream, ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps or 20
+    ms = []
+    for _ in range(K):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    st, detail = bsm.bsm_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+    mean = statistics.fmean(ms)
+    peaks = load_peaks()
+    tf = flops / (mean * 1e-3) / 1e12
+    nnz = int(info.row_ptr[-1].item())
+    per_table = w.H if info.struct.num_tables > 1 else w.B * w.H
+    executed = nnz * w.block_q * w.block_kv * 2 * w.D * 7 * per_table
+    return {
+        "metric": "masked-attn bwd TFLOP/s (unmasked FLOPs, 5 products per "
+                  "visible pair)",
+        "value": round(tf, 2), "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(mean, 5),
+        "higher_is_better": True, "dtype": "bf16",
+        "config": dict(config_block(w, seg, flops), parallelism="single GPU"),
+        "roofline": {"kernel": "splash_bwd_kernel (dK/dV, dQ) + D_q",
+                     "bound": "tensor", "achieved": round(tf, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "executed_mma_flops": executed},
+        "gpu_launches": 3 * K if sm else 2 * K,
+    }
+
+
 def mask_info_bytes(w, info):
     """Algorithmic HBM bytes of one mask-info build: segment ids read once,
     every table written once (block classes, next-block table, CSR offsets,
@@ -643,6 +722,14 @@ def main(argv=None):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     names = list(wl.WORKLOADS) if args.all else [args.workload]
+    if args.bwd:
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        for name in names:
+            if rank == 0:
+                print(json.dumps(run_bwd(args, wl.WORKLOADS[name], dev)),
+                      flush=True)
+        return 0
     for name in names:
         w = wl.WORKLOADS[name]
         line = run_ours(args, w, world, rank, local)

@@ -118,21 +118,78 @@ __device__ __forceinline__ int bwd_tile_class(const BwdParams& p, int table,
   return 1;
 }
 
-// Visibility of (query q, key k) under every predicate of the mask (the
-// mask-info builder applies the same ones).
-__device__ __forceinline__ bool bwd_visible(const BwdParams& p, int b, int q,
-                                            int k) {
-  bool v = q < p.Sq && k < p.Skv;
-  if (p.flags & BSM_MASK_CAUSAL) v = v && (k <= q);
-  if (p.flags & BSM_MASK_LOCAL) v = v && (q - k < p.window);
-  if (p.flags & BSM_MASK_BAND) v = v && (k - q < p.window);
-  if (v && (p.flags & BSM_MASK_SEGMENT))
-    v = p.q_seg[static_cast<int64_t>(b) * p.Sq + q] ==
-        p.kv_seg[static_cast<int64_t>(b) * p.Skv + k];
-  if (v && p.dense != nullptr)
-    v = (__ldg(p.dense + static_cast<int64_t>(q) * p.dense_words + (k >> 5)) >>
-         (k & 31)) & 1u;
-  return v;
+// Bits of the columns [lo, hi] within the 32 columns starting at c0.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int c0) {
+  const int lb = min(max(lo - c0, 0), 32), hb = min(max(hi - c0 + 1, 0), 32);
+  const uint32_t below_hi = hb >= 32 ? 0xffffffffu : (1u << hb) - 1u;
+  const uint32_t below_lo = lb >= 32 ? 0xffffffffu : (1u << lb) - 1u;
+  return below_hi & ~below_lo;
+}
+
+// Visibility bits of one thread's row against 32 consecutive columns
+// starting at c0 (a multiple of 32), under every predicate of the mask (the
+// ones the mask-info builder applies).  DKDV: the row is key `row` and the
+// columns are queries; dQ: the row is query `row` and the columns are keys.
+// Causal/local/band and the sequence ends are a range of columns; segment
+// ids and arbitrary-mask words of the 32 columns are loaded one per lane
+// and passed around with shuffles.  Whole warp.
+template <bool DKDV>
+__device__ __forceinline__ uint32_t chunk_visible(const BwdParams& p, int b,
+                                                  int row, int row_seg,
+                                                  int c0) {
+  const int lane = threadIdx.x % 32;
+  int lo, hi;
+  if (DKDV) {  // queries q that see key k = row
+    const int k = row;
+    lo = 0;
+    hi = p.Sq - 1;
+    if (p.flags & BSM_MASK_CAUSAL) lo = max(lo, k);
+    if (p.flags & BSM_MASK_LOCAL) hi = min(hi, k + p.window - 1);
+    if (p.flags & BSM_MASK_BAND) lo = max(lo, k - p.window + 1);
+    if (k >= p.Skv) hi = -1;
+  } else {  // keys k that query q = row sees
+    const int q = row;
+    lo = 0;
+    hi = p.Skv - 1;
+    if (p.flags & BSM_MASK_CAUSAL) hi = min(hi, q);
+    if (p.flags & BSM_MASK_LOCAL) lo = max(lo, q - p.window + 1);
+    if (p.flags & BSM_MASK_BAND) hi = min(hi, q + p.window - 1);
+    if (q >= p.Sq) hi = -1;
+  }
+  uint32_t bits = range_bits(lo, hi, c0);
+  const int col = c0 + lane;  // this lane's column
+  if (p.flags & BSM_MASK_SEGMENT) {
+    int cs = 0;
+    if (DKDV ? col < p.Sq : col < p.Skv)
+      cs = DKDV ? p.q_seg[static_cast<int64_t>(b) * p.Sq + col]
+                : p.kv_seg[static_cast<int64_t>(b) * p.Skv + col];
+    uint32_t same = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      same |= (__shfl_sync(0xffffffffu, cs, j) == row_seg ? 1u : 0u) << j;
+    bits &= same;
+  }
+  if (p.dense != nullptr) {
+    if (DKDV) {
+      // word (query col, keys of this warp): the warp's 32 keys share it
+      const int kw = (row - lane) >> 5;
+      uint32_t w = 0;
+      if (col < p.Sq && kw * 32 < p.Skv)
+        w = __ldg(p.dense + static_cast<int64_t>(col) * p.dense_words + kw);
+      uint32_t keep = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        keep |= ((__shfl_sync(0xffffffffu, w, j) >> lane) & 1u) << j;
+      bits &= keep;
+    } else {
+      uint32_t w = 0;
+      if (row < p.Sq && c0 < p.Skv)
+        w = __ldg(p.dense + static_cast<int64_t>(row) * p.dense_words +
+                  (c0 >> 5));
+      bits &= w;
+    }
+  }
+  return bits;
 }
 
 // The CTA's list of nonzero tiles (uint16: tile << 2 | class), built by one
@@ -335,6 +392,11 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
   const float kLog2e = 1.4426950408889634f;
   // the thread's row: a key (dK/dV) or a query (dQ)
   const int row = fixed_tile * kTileM + r;
+  // the row's segment id (the thread's key or query)
+  int row_seg = 0;
+  if ((p.flags & BSM_MASK_SEGMENT) && (DKDV ? row < p.Skv : row < p.Sq))
+    row_seg = DKDV ? p.kv_seg[static_cast<int64_t>(b) * p.Skv + row]
+                   : p.q_seg[static_cast<int64_t>(b) * p.Sq + row];
   // dQ: the row's lse (log2 units) and D_q are fixed
   float lse2_row = 0.f, delta_row = 0.f;
   if (!DKDV && SCORE == BSM_SCORE_SOFTMAX && row < p.Sq) {
@@ -369,16 +431,9 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
         delta_c = p.delta[i];
       }
       // visibility bits of the chunk (partial tiles only)
-      uint32_t vis = 0xffffffffu;
-      if (cls == 1) {
-        vis = 0u;
-        for (int j = 0; j < 32; ++j) {
-          const int cidx = col0 + c * 32 + j;
-          const bool v = DKDV ? bwd_visible(p, b, cidx, row)
-                              : bwd_visible(p, b, row, cidx);
-          vis |= (v ? 1u : 0u) << j;
-        }
-      }
+      const uint32_t vis =
+          cls == 1 ? chunk_visible<DKDV>(p, b, row, row_seg, col0 + c * 32)
+                   : 0xffffffffu;
       tmem_ld_wait();
       uint32_t pw[16], dsw[16];
 #pragma unroll
