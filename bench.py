@@ -124,8 +124,9 @@ def rank_workload(w, world: int, rank: int, strong: bool):
     problem has world*H heads and rank r owns [r*H, (r+1)*H), drawn with
     its own seed.  Strong: the workload's H heads are partitioned."""
     if strong:
-        h0, h1 = head_partition(w.H, world, rank)
-        return w.with_(H=h1 - h0), h0, h1, w.H
+        g = w.H // w.Hkv_  # query heads per K/V head stay together
+        h0, h1 = head_partition(w.H, world, rank, g)
+        return (w.with_(H=h1 - h0, Hkv=(h1 - h0) // g), h0, h1, w.H)
     h0, h1 = head_partition(world * w.H, world, rank)
     return w.with_(seed=rank_seed(w, rank)), h0, h1, world * w.H
 
@@ -270,7 +271,8 @@ def workload_flops(w, seg):
 
 
 def config_block(w, seg, flops):
-    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+    return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv_,
+            "S": w.S, "D": w.D,
             "mask": mask_name(w.flags, w.window),
             "score": "softmax" if w.score == wl.SCORE_SOFTMAX
             else "hstu_pointwise",
@@ -291,7 +293,10 @@ def run_ours(args, w, world, rank, local):
     # row, shared by every head, so every rank uses the same ones
     w, h0, h1, H_global = rank_workload(wfull, world, rank, args.strong)
     if args.strong:
-        q, k, v = (t[:, h0:h1].contiguous() for t in wl.make_qkv(wfull))
+        g = wfull.H // wfull.Hkv_
+        qf, kf, vf = wl.make_qkv(wfull)
+        q = qf[:, h0:h1].contiguous()
+        k, v = (t[:, h0 // g:h1 // g].contiguous() for t in (kf, vf))
     else:
         q, k, v = wl.make_qkv(w)
     seg = wl.make_segment_ids(w)
@@ -571,7 +576,7 @@ def forward_roofline(w, flops, fwd_ms, peaks, traffic):
 def algorithmic_bytes(w):
     """q, k, v, out once each (bf16) plus lse (f32)."""
     qo = 2 * w.B * w.H * w.Sq * w.D * 2
-    kv = 2 * w.B * w.H * w.Skv_ * w.D * 2
+    kv = 2 * w.B * w.Hkv_ * w.Skv_ * w.D * 2
     lse = 4 * w.B * w.H * w.Sq if w.score == wl.SCORE_SOFTMAX else 0
     return qo + kv + lse
 
@@ -624,6 +629,10 @@ def run_e2e(args, w, q, k, v, seg, flops, dev):
 def oracle_head(w, q, k, v, seg, b, h):
     """Run the fp64 oracle on every row of one (batch, head)."""
     import oracle
+
+    if k.shape[1] != q.shape[1]:  # grouped K/V heads: the oracle takes one
+        g = q.shape[1] // k.shape[1]  # K/V head per query head
+        k, v = k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1)
 
     rows = [(b, h, r) for r in range(w.Sq)]
     dm = wl.make_dense_mask(w)

@@ -60,6 +60,7 @@ class Workload:
     seg_max: int = 2048
     Skv: int | None = None  # None: same as S
     dense_p: float = 0.5    # MASK_DENSE: P(visible) inside random tiles
+    Hkv: int | None = None  # K/V heads (None: H); H must be a multiple
 
     @property
     def Sq(self) -> int:
@@ -68,6 +69,10 @@ class Workload:
     @property
     def Skv_(self) -> int:
         return self.S if self.Skv is None else self.Skv
+
+    @property
+    def Hkv_(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -116,6 +121,11 @@ WORKLOADS: dict[str, Workload] = {
         "next2_dense_s8192_d128", 2, 16, 8192, 128, 128, 128,
         MASK_DENSE | MASK_CAUSAL, 0, SCORE_SOFTMAX, 1.0 / math.sqrt(128), 1.0,
         1007),
+    # grouped-query attention: 32 query heads over 8 K/V heads, causal,
+    # B=2 S=8192 D=128
+    "next1_gqa_s8192_d128": Workload(
+        "next1_gqa_s8192_d128", 2, 32, 8192, 128, 128, 128, MASK_CAUSAL, 0,
+        SCORE_SOFTMAX, 1.0 / math.sqrt(128), 1.0, 1008, Hkv=8),
 }
 
 # The configuration the headline throughput is quoted on (causal, S=8192,
@@ -124,7 +134,8 @@ HEADLINE = "cfg3_packed_s8192_d128"
 
 
 def make_qkv(w: Workload, B: int | None = None, H: int | None = None):
-    """q, k, v as CPU bfloat16 tensors [B, H, S, D] (contiguous).
+    """q [B, H, Sq, D], k and v [B, H_kv, Skv, D] as CPU bfloat16 tensors
+    (contiguous).
 
     ``B``/``H`` may be reduced to draw a prefix-shaped sample; the values of
     the full-size draw are not reproduced in that case (the generator stream
@@ -135,11 +146,12 @@ def make_qkv(w: Workload, B: int | None = None, H: int | None = None):
     H = w.H if H is None else H
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
+    Hkv = H * w.Hkv_ // w.H  # K/V heads in the same ratio
     q = (torch.randn((B, H, w.Sq, w.D), generator=g, dtype=torch.float32)
          * w.sigma).to(torch.bfloat16)
-    k = (torch.randn((B, H, w.Skv_, w.D), generator=g, dtype=torch.float32)
+    k = (torch.randn((B, Hkv, w.Skv_, w.D), generator=g, dtype=torch.float32)
          * w.sigma).to(torch.bfloat16)
-    v = (torch.randn((B, H, w.Skv_, w.D), generator=g, dtype=torch.float32)
+    v = (torch.randn((B, Hkv, w.Skv_, w.D), generator=g, dtype=torch.float32)
          * w.sigma).to(torch.bfloat16)
     return q, k, v
 

@@ -395,3 +395,23 @@ def test_many_repeats_bitwise_identical(score):
         want = oracle.pointwise_attention(q, k, v, C, 0, None, None, 0.09,
                                           rows=rows)
         compare_out(got, want, pointwise=True, what="repeat")
+
+
+def test_full_size_grouped_heads_every_row_of_sampled_heads():
+    # 32 query heads over 8 K/V heads: units pair two heads of a group on
+    # the same rows.  Every row of heads from both members of a pair and
+    # of different groups and batch rows, against the oracle with the
+    # matching K/V head ([NOTES] section 21: head h reads K/V head h // 4).
+    name = "next1_gqa_s8192_d128"
+    w, q, k, v, seg = workload_inputs(name)
+    out, lse, _ = run_gpu(q, k, v, w.flags, w.window, seg, seg, w.scale,
+                          w.score)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    G = w.H // w.Hkv_
+    for (b, h) in [(0, 0), (0, 1), (0, 6), (1, 19), (1, 31)]:
+        kh = slice(h // G, h // G + 1)
+        ref, ref_lse = oracle.softmax_attention(
+            q[b:b + 1, h:h + 1], k[b:b + 1, kh], v[b:b + 1, kh], w.flags,
+            w.window, None, None, w.scale)
+        compare_out(out[b:b + 1, h:h + 1].numpy(), ref, what=f"b{b} h{h}")
+        compare_lse(lse[b:b + 1, h:h + 1].numpy(), ref_lse, what=f"b{b} h{h}")
