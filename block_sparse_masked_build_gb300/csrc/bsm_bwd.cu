@@ -23,11 +23,11 @@
 //          tiles of its row, as the forward does, and accumulates dQ.
 // A third, small kernel computes D_q (softmax path only).
 //
-// Warp roles (192 threads): warp 0 loads with TMA (the CTA's fixed pair of
+// Warp roles (320 threads): warp 0 loads with TMA (the CTA's fixed pair of
 // tiles once, then the streamed pair of every step through a two-stage
 // ring), warp 1 issues the tcgen05 MMAs (lane 0) and owns the TMEM
-// allocation, warps 2-5 do the elementwise work, one thread per TMEM lane
-// (a row of the fixed tiles).  Per step, with F0/F1 the fixed tiles and
+// allocation, warps 2-9 do the elementwise work, a thread per TMEM lane (a
+// row of the fixed tiles) and column half.  Per step, with F0/F1 the fixed tiles and
 // T0/T1 the streamed ones (dK/dV: F = K, V and T = Q, dO; dQ: F = Q, dO and
 // T = K, V):
 //     S  = F0 T0^T   -> TMEM [0, 128)      (both operands K-major in smem)
@@ -51,7 +51,7 @@ __device__ int g_bwd_error[4];
 
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;  // warps 0-1 roles, 2-9 elementwise
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr int kRoleBLoad = 11, kRoleBMma = 12, kRoleBElem = 13;
 
@@ -71,6 +71,7 @@ struct BwdBars {
   uint64_t f_full;
   uint64_t t_full[2], t_empty[2];
   uint64_t s_full, dp_full, p_ready, acc_done, mma_done;
+  uint64_t h0_read;  // the first column half has read S and dP
   uint32_t tmem_base;
   int abort;
   int n_list;
@@ -373,7 +374,11 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
   __syncwarp();
 }
 
-// Elementwise warps: one thread per row of the fixed tiles (TMEM lane).
+// Elementwise warps: two per TMEM lane quarter (one thread per row of the
+// fixed tiles), warps 2-5 taking columns [0, 64) of S and dP, warps 6-9
+// columns [64, 128).  The packed P and dS of the second half go over
+// columns [32, 64), which the first half reads: the second half writes only
+// after the first half has read (h0_read).
 template <int D, int SCORE, bool DKDV>
 __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
                                               BwdBars* bars,
@@ -383,6 +388,7 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
                                               int n_iter) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quarter = warp % 4;  // TMEM lanes this warp may access
+  const int half = (warp - 2) / 4;  // column half of S and dP
   const int r = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
@@ -409,7 +415,7 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
     const int e = it % n_list;
     const int tile = list[e] >> 2, cls = list[e] & 3;
     const int head = DKDV ? hq_or_hkv * G + it / n_list : hq_or_hkv;
-    const int col0 = tile * kTileM;  // first query (dK/dV) / key (dQ)
+    const int col0 = tile * kTileM + half * 64;  // first column of the half
     ok = bwarp_wait(&bars->s_full, it & 1, abort_flag, p.timeout_ns) &&
          bwarp_wait(&bars->dp_full, it & 1, abort_flag, p.timeout_ns);
     if (!ok) {
@@ -417,62 +423,76 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
       break;
     }
     tc_fence_after();
-#pragma unroll 1
-    for (int c = 0; c < kTileN / 32; ++c) {
-      uint32_t sraw[32], dpraw[32];
-      tmem_ld32(t_s + c * 32, sraw);
-      tmem_ld32(t_dp + c * 32, dpraw);
-      // per-column statistics of the 32 queries of this chunk (dK/dV)
-      float lse2_c = 0.f, delta_c = 0.f;
+    uint32_t sraw[64], dpraw[64];
+    tmem_ld32(t_s + half * 64, sraw);
+    tmem_ld32(t_s + half * 64 + 32, sraw + 32);
+    tmem_ld32(t_dp + half * 64, dpraw);
+    tmem_ld32(t_dp + half * 64 + 32, dpraw + 32);
+    // per-column statistics and visibility of the half's 64 columns
+    float lse2_c[2] = {0.f, 0.f}, delta_c[2] = {0.f, 0.f};
+    uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
       const int qc = col0 + c * 32 + lane;
       if (DKDV && SCORE == BSM_SCORE_SOFTMAX && qc < p.Sq) {
         const int64_t i = (static_cast<int64_t>(b) * p.H + head) * p.Sq + qc;
-        lse2_c = p.lse[i] * kLog2e;
-        delta_c = p.delta[i];
+        lse2_c[c] = p.lse[i] * kLog2e;
+        delta_c[c] = p.delta[i];
       }
-      // visibility bits of the chunk (partial tiles only)
-      const uint32_t vis =
-          cls == 1 ? chunk_visible<DKDV>(p, b, row, row_seg, col0 + c * 32)
-                   : 0xffffffffu;
-      tmem_ld_wait();
-      uint32_t pw[16], dsw[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float pv[2], dsv[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float sv = __uint_as_float(sraw[j + u]);
-          const float dpv = __uint_as_float(dpraw[j + u]);
-          const bool v = (vis >> (j + u)) & 1u;
-          if (SCORE == BSM_SCORE_SOFTMAX) {
-            const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c, j + u)
-                                  : lse2_row;
-            const float dl = DKDV ? __shfl_sync(0xffffffffu, delta_c, j + u)
-                                  : delta_row;
-            const float pr = v ? ex2_approx(fmaf(sv, p.scale_log2, -l2)) : 0.f;
-            pv[u] = pr;
-            dsv[u] = pr * (dpv - dl);
-          } else {
-            const float x = sv * p.scale;
-            const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-            pv[u] = v ? x * sig * p.inv_sq : 0.f;
-            dsv[u] = v ? dpv * sig * fmaf(x, 1.f - sig, 1.f) * p.inv_sq : 0.f;
-          }
-        }
-        pw[j / 2] = pack_bf16x2(pv[0], pv[1]);
-        dsw[j / 2] = pack_bf16x2(dsv[0], dsv[1]);
-      }
-      // P over S's columns, dS over dP's: chunk c writes columns 16c..16c+15,
-      // which this or an earlier chunk has already read
-      if (DKDV) tmem_st16(t_s + c * 16, pw);
-      tmem_st16(t_dp + c * 16, dsw);
+      if (cls == 1) vis[c] = chunk_visible<DKDV>(p, b, row, row_seg, col0 + c * 32);
     }
+    tmem_ld_wait();
+    if (half == 0) {
+      tc_fence_before();
+      mbar_arrive(&bars->h0_read);
+    }
+    uint32_t pw[32], dsw[32];
+#pragma unroll
+    for (int j = 0; j < 64; j += 2) {
+      float pv[2], dsv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = (j + u) >> 5, jj = (j + u) & 31;
+        const float sv = __uint_as_float(sraw[j + u]);
+        const float dpv = __uint_as_float(dpraw[j + u]);
+        const bool v = (vis[c] >> jj) & 1u;
+        if (SCORE == BSM_SCORE_SOFTMAX) {
+          const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c[c], jj)
+                                : lse2_row;
+          const float dl = DKDV ? __shfl_sync(0xffffffffu, delta_c[c], jj)
+                                : delta_row;
+          const float pr = v ? ex2_approx(fmaf(sv, p.scale_log2, -l2)) : 0.f;
+          pv[u] = pr;
+          dsv[u] = pr * (dpv - dl);
+        } else {
+          const float x = sv * p.scale;
+          const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+          pv[u] = v ? x * sig * p.inv_sq : 0.f;
+          dsv[u] = v ? dpv * sig * fmaf(x, 1.f - sig, 1.f) * p.inv_sq : 0.f;
+        }
+      }
+      pw[j / 2] = pack_bf16x2(pv[0], pv[1]);
+      dsw[j / 2] = pack_bf16x2(dsv[0], dsv[1]);
+    }
+    if (half == 1) {  // columns [32, 64) are the first half's input
+      if (!bwarp_wait(&bars->h0_read, it & 1, abort_flag, p.timeout_ns)) {
+        record_bwd_timeout(kRoleBElem, 2);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+    }
+    // P over S's columns, dS over dP's: the half's 64 columns pack into
+    // columns 32 * half .. 32 * half + 31
+    if (DKDV) tmem_st32(t_s + half * 32, pw);
+    tmem_st32(t_dp + half * 32, dsw);
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&bars->p_ready);
   }
   if (!ok) return;
-  // ---- results: dK/dV rows (keys) or dQ rows, bf16; dK and dQ scaled
+  // ---- results: dK/dV rows (keys) or dQ rows, bf16; dK and dQ scaled;
+  // each half stores half of the D columns
   const bool row_ok = DKDV ? row < p.Skv : row < p.Sq;
   if (n_iter > 0) {
     if (!bwarp_wait(&bars->acc_done, 0, abort_flag, p.timeout_ns)) {
@@ -499,7 +519,7 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
       mul = p.scale;
     }
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
       uint32_t o[32];
       if (n_iter > 0) {
         tmem_ld32(tmem + lane_off + 256 + a * 128 + c * 32, o);
@@ -552,7 +572,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->h0_read, 128);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
