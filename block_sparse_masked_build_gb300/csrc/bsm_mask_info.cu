@@ -21,9 +21,10 @@
 //      area.  Then it takes a ticket; the CTA that finishes last turns the
 //      counts into CSR row offsets, ORs the tables' "not sorted" bits into
 //      seg_flags[0] and orders the super-tiles (finish_tables).  The ticket
-//      word is (epoch, count): each build brings a new epoch, so no reset
-//      between builds is needed and a stale word from an earlier build, or
-//      garbage, is never counted.
+//      word is (epoch, count): each build brings a new epoch, installed by
+//      the first CTA to start, so a stale word from an earlier build, or
+//      garbage, is never counted; the last CTA puts the count back to zero,
+//      so a replay of the same launch (same epoch) starts from zero too.
 //   copy: a warp per row moves the staged list to its CSR place.  Launched
 //      with programmatic stream serialization, so it is scheduled while
 //      classify runs and waits (griddepcontrol.wait) for its completion.
@@ -102,7 +103,8 @@ __device__ __forceinline__ bool base_visible(const MaskInfoParams& p, int q,
 struct FinishScratch {
   int warp_sums[32];
   int carry;
-  unsigned long long wmax;
+  uint32_t wmax;
+  int any_unsorted;
 };
 
 // Run by one CTA (any multiple of 32 threads): inclusive scan of the row
@@ -111,22 +113,46 @@ struct FinishScratch {
 // order in which the forward should take its 256-row super-tiles: by
 // decreasing work (sum over the super-tile's rows of the nonzero blocks they
 // see), so that the longest units start first and the short ones fill in at
-// the end.  `keys` holds kMaxSuperOrder words of shared memory.
-__device__ void finish_tables(const MaskInfoParams& p, FinishScratch& fs,
-                              uint32_t* keys) {
+// the end.  `keys` holds kMaxSuperOrder words of shared memory; the work of
+// each (table, super-tile) pair is summed there while the counts are scanned
+// and then turned into its sort key in place.
+__device__ __forceinline__ void finish_tables(const MaskInfoParams& p,
+                                              FinishScratch& fs,
+                                              uint32_t* keys) {
   int32_t* row_ptr = p.row_ptr;
   const int R = p.tables * p.nq;
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int nwarps = blockDim.x / 32;
+  const bool order = p.super_order != nullptr;
+  const int pairs = p.tables * p.n_super;  // <= kMaxSuperOrder when ordered
+  // the "not sorted" bits are read alongside the first counts
+  int unsorted = 0;
+  if (p.flags & BSM_MASK_SEGMENT)
+    for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
+      unsorted |= p.seg_flags[1 + tb];
+  if (order)
+    for (int i = threadIdx.x; i < pairs; i += blockDim.x) keys[i] = 0;
   if (threadIdx.x == 0) {
     row_ptr[0] = 0;
     fs.carry = 0;
     fs.wmax = 0;
   }
+  fs.any_unsorted = 0;
   __syncthreads();
+  if (unsorted) fs.any_unsorted = 1;
   for (int base = 0; base < R; base += blockDim.x) {
     const int idx = base + threadIdx.x;
-    int v = idx < R ? row_ptr[idx + 1] : 0;
+    const int cnt = idx < R ? row_ptr[idx + 1] : 0;
+    if (order && idx < R && cnt > 0) {
+      // this block row's share of each super-tile it overlaps
+      const int t = idx / p.nq, i = idx - t * p.nq;
+      const int r0 = i * p.bq, r1 = min(p.Sq, r0 + p.bq);  // [r0, r1)
+      for (int st = r0 / kUnitRows; st * kUnitRows < r1; ++st) {
+        const int rows = min(r1, (st + 1) * kUnitRows) - max(r0, st * kUnitRows);
+        atomicAdd(&keys[t * p.n_super + st], static_cast<uint32_t>(cnt * rows));
+      }
+    }
+    int v = cnt;
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, v, o);
       if (lane >= o) v += n;
@@ -149,30 +175,16 @@ __device__ void finish_tables(const MaskInfoParams& p, FinishScratch& fs,
     if (threadIdx.x == blockDim.x - 1) fs.carry = carry + fs.warp_sums[nwarps - 1];
     __syncthreads();
   }
-  if (p.flags & BSM_MASK_SEGMENT) {  // any table's kv ids not sorted
-    int any = 0;
-    for (int tb = threadIdx.x; tb < p.tables; tb += blockDim.x)
-      any |= p.seg_flags[1 + tb];
-    any = __syncthreads_or(any);
-    if (threadIdx.x == 0) p.seg_flags[0] = any ? 1 : 0;
-  }
-  if (p.super_order == nullptr) return;
+  __syncthreads();
+  if ((p.flags & BSM_MASK_SEGMENT) && threadIdx.x == 0)
+    p.seg_flags[0] = fs.any_unsorted;
+  if (!order) return;
 
   // ---- longest-first order of the (table, super-tile) pairs
-  const int pairs = p.tables * p.n_super;  // <= kMaxSuperOrder
-  auto work = [&](int pr) -> unsigned long long {
-    const int t = pr / p.n_super, st = pr % p.n_super;
-    const int r0 = st * kUnitRows, r1 = min(p.Sq, r0 + kUnitRows);
-    unsigned long long w = 0;
-    for (int i = r0 / p.bq; i <= (r1 - 1) / p.bq; ++i) {
-      const int cnt = row_ptr[t * p.nq + i + 1] - row_ptr[t * p.nq + i];
-      const int rows = min(r1, (i + 1) * p.bq) - max(r0, i * p.bq);
-      w += static_cast<unsigned long long>(cnt) * rows;
-    }
-    return w;
-  };
-  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x)
-    atomicMax(&fs.wmax, work(pr));
+  uint32_t wm = 0;
+  for (int pr = threadIdx.x; pr < pairs; pr += blockDim.x) wm = max(wm, keys[pr]);
+  for (int o = 16; o > 0; o >>= 1) wm = max(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  if (lane == 0 && wm > 0) atomicMax(&fs.wmax, wm);
   __syncthreads();
   const unsigned long long wmax = fs.wmax > 0 ? fs.wmax : 1;
   int n2 = 1;
@@ -183,7 +195,7 @@ __device__ void finish_tables(const MaskInfoParams& p, FinishScratch& fs,
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
     uint32_t key = 0xffffffffu;
     if (i < pairs) {
-      const unsigned long long q = work(i) * 0x7ffffull / wmax;
+      const unsigned long long q = keys[i] * 0x7ffffull / wmax;
       key = (static_cast<uint32_t>(0x7ffffull - q) << 13) |
             (0x1fffu - static_cast<uint32_t>(i));
     }
@@ -228,6 +240,43 @@ __global__ void __launch_bounds__(kMiThreads)
   // grid's completion before reading anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // Ticket, part one: install this build's epoch if the word still holds
+  // another one.  Issued first so that its round trips overlap the loads
+  // below; the same thread counts this CTA at the end, after it.
+  if (p.fused && threadIdx.x == 0) {
+    const unsigned long long mine = p.epoch << kTicketBits;
+    const unsigned long long cur =
+        *reinterpret_cast<volatile unsigned long long*>(p.ticket);
+    if ((cur >> kTicketBits) != p.epoch) atomicCAS(p.ticket, cur, mine);
+  }
+
+  // The kv ids of this table are staged in shared memory when they fit; their
+  // loads are issued together with the row block's q ids, so that one
+  // barrier covers both.
+  const int32_t* ks = nullptr;
+  const bool staged = seg && p.Skv <= kStagedKeys;
+  if (seg) {
+    const int32_t* ks_g = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
+    ks = ks_g;
+    if (staged) {
+      int32_t* ks_s = reinterpret_cast<int32_t*>(dyn_s + cls_bytes(p.nk));
+      // 16-byte loads, unrolled so that all of a thread's loads are in
+      // flight at once (the ids of a table are read by every row's CTA)
+      int k0 = 0;
+      if ((reinterpret_cast<uintptr_t>(ks_g) & 15u) == 0) {
+        const int n4 = p.Skv / 4;
+        const int4* g4 = reinterpret_cast<const int4*>(ks_g);
+        int4* s4 = reinterpret_cast<int4*>(ks_s);
+#pragma unroll 8
+        for (int k = threadIdx.x; k < n4; k += blockDim.x) s4[k] = __ldg(g4 + k);
+        k0 = 4 * n4;
+      }
+      for (int k = k0 + threadIdx.x; k < p.Skv; k += blockDim.x)
+        ks_s[k] = ks_g[k];
+      ks = ks_s;
+    }
+  }
+
   int qmin = kPosInf, qmax = kNegInf;
   if (seg) {
     const int32_t* qs = p.q_seg + static_cast<int64_t>(t) * p.Sq;
@@ -257,48 +306,27 @@ __global__ void __launch_bounds__(kMiThreads)
     }
   }
 
-  // kv ids of this table: staged in shared memory when they fit
-  const int32_t* ks = nullptr;
   bool sorted = true;
   if (seg) {
-    const int32_t* ks_g = p.kv_seg + static_cast<int64_t>(t) * p.Skv;
-    ks = ks_g;
-    if (p.Skv <= kStagedKeys) {
-      int32_t* ks_s = reinterpret_cast<int32_t*>(dyn_s + cls_bytes(p.nk));
-      // 16-byte loads, unrolled so that all of a thread's loads are in
-      // flight at once (the ids of a table are read by every row's CTA)
-      int k0 = 0;
-      if ((reinterpret_cast<uintptr_t>(ks_g) & 15u) == 0) {
-        const int n4 = p.Skv / 4;
-        const int4* g4 = reinterpret_cast<const int4*>(ks_g);
-        int4* s4 = reinterpret_cast<int4*>(ks_s);
-#pragma unroll 8
-        for (int k = threadIdx.x; k < n4; k += blockDim.x) s4[k] = __ldg(g4 + k);
-        k0 = 4 * n4;
-      }
-      for (int k = k0 + threadIdx.x; k < p.Skv; k += blockDim.x)
-        ks_s[k] = ks_g[k];
-      __syncthreads();
-      ks = ks_s;
-    }
     bool unsorted = false;
 #pragma unroll 8
     for (int k = threadIdx.x; k + 1 < p.Skv; k += blockDim.x)
       unsorted |= ks[k] > ks[k + 1];
     sorted = !__syncthreads_or(unsorted);
     if (i == 0 && threadIdx.x == 0) p.seg_flags[1 + t] = sorted ? 0 : 1;
-    // each row's [first, last] key with its id (first > last: none)
-    int2* sr_g = reinterpret_cast<int2*>(p.seg_range) +
-                 static_cast<int64_t>(t) * p.Sq;
-    for (int r = r0 + threadIdx.x; r <= r1; r += blockDim.x) {
-      const int v = qseg_s[r - r0];
-      int2 rg;
-      rg.x = id_search(ks, p.Skv, v, false);
-      rg.y = id_search(ks, p.Skv, v, true) - 1;
-      sr_s[r - r0] = rg;
-      sr_g[r] = rg;
+    // each row's [first, last] key with its id (first > last: none); the
+    // two searches of a row run on different threads
+    const int nrows = r1 - r0 + 1;
+    for (int e = threadIdx.x; e < 2 * nrows; e += blockDim.x) {
+      const bool after = e >= nrows;
+      const int r = after ? e - nrows : e;
+      const int x = id_search(ks, p.Skv, qseg_s[r], after);
+      if (after) sr_s[r].y = x - 1; else sr_s[r].x = x;
     }
     __syncthreads();
+    int2* sr_g = reinterpret_cast<int2*>(p.seg_range) +
+                 static_cast<int64_t>(t) * p.Sq;
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) sr_g[r0 + r] = sr_s[r];
   }
   const bool ranges = seg && sorted;
 
@@ -467,24 +495,20 @@ __global__ void __launch_bounds__(kMiThreads)
   }
   if (!p.fused) return;
 
-  // ---- ticket: the CTA that finishes last completes the tables.  Every
-  // thread's writes are made visible device-wide before the CTA counts
+  // ---- ticket, part two: the CTA that finishes last completes the tables.
+  // Every thread's writes are made visible device-wide before the CTA counts
   // itself; the word holds (epoch << kTicketBits) | CTAs counted, so a word
-  // from an earlier build (another epoch) counts as zero.
+  // from an earlier build (another epoch) counts as zero.  Each CTA installed
+  // the epoch (or found it installed) before counting, and within a build
+  // only that swap changes the epoch, so no count is lost to it.  The last
+  // CTA puts the count back to zero, so that a replay of the same launch
+  // (same epoch) counts from zero as well.
   __shared__ int last_s;
   __shared__ FinishScratch fs;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    // Install this build's epoch if the word still holds another one (the
-    // first CTA to get here does; a CTA whose swap fails finds it done:
-    // within a build only this swap changes the epoch, and counting starts
-    // after it), then count with one atomic add.
     const int total = p.nq * p.tables;
-    const unsigned long long mine = p.epoch << kTicketBits;
-    unsigned long long cur =
-        *reinterpret_cast<volatile unsigned long long*>(p.ticket);
-    if ((cur >> kTicketBits) != p.epoch) atomicCAS(p.ticket, cur, mine);
     const unsigned long long got = atomicAdd(p.ticket, 1ull);
     const bool ok = (got >> kTicketBits) == p.epoch;
     last_s = (ok && static_cast<int>(got & ((1ull << kTicketBits) - 1)) ==
@@ -493,6 +517,7 @@ __global__ void __launch_bounds__(kMiThreads)
   }
   __syncthreads();
   if (!last_s) return;
+  if (threadIdx.x == 0) atomicExch(p.ticket, p.epoch << kTicketBits);
   finish_tables(p, fs, reinterpret_cast<uint32_t*>(dyn_s));
 }
 
