@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     bsm_device_status,
     bsm_last_error,
     bsm_mask_info_bytes,
+    bsm_pack_dense_mask,
     bsm_selftest_wait_timeout,
     bsm_splash_bwd,
     bsm_splash_bwd_workspace_bytes,

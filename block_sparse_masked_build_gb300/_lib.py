@@ -29,7 +29,7 @@ STATUS_NAMES = {
 }
 
 
-ABI_VERSION = 300  # the struct layouts below
+ABI_VERSION = 301  # the struct layouts below
 
 
 class MaskSpec(ctypes.Structure):
@@ -110,6 +110,10 @@ def _declare(lib):
         c.c_int32, c.c_int32, c.c_int32, c.POINTER(MaskInfoStruct),
         c.c_void_p, c.c_void_p, c.c_float, c.c_int32, tv, tv, tv, c.c_void_p,
         c.c_size_t, c.c_void_p]
+    lib.bsm_pack_dense_mask.restype = c.c_int
+    lib.bsm_pack_dense_mask.argtypes = [c.c_void_p, c.c_int64, c.c_int32,
+                                        c.c_int32, c.c_void_p, c.c_int32,
+                                        c.c_void_p]
     lib.bsm_device_status.restype = c.c_int
     lib.bsm_device_status.argtypes = [c.c_void_p, c.POINTER(c.c_int32)]
     lib.bsm_selftest_wait_timeout.restype = c.c_int

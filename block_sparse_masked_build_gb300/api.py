@@ -325,21 +325,37 @@ def build_mask_info(flags: int, B: int, Sq: int, Skv: int, block_q: int = 128,
                                dense_bits)
 
 
-def pack_dense_mask(mask: torch.Tensor) -> torch.Tensor:
-    """Bit-pack a boolean [Sq, Skv] device mask into int32 words [Sq, W],
-    W = ceil(Skv / 32): bit k % 32 of word k // 32 of row q is mask[q, k]
-    (the layout BSM_MASK_DENSE reads)."""
+def bsm_pack_dense_mask(mask: torch.Tensor, words: torch.Tensor,
+                        stream=None) -> None:
+    """Bit-pack a boolean CUDA mask [Sq, Skv] (rows contiguous) into the
+    int32/uint32 CUDA tensor words [Sq, W], W >= ceil(Skv / 32): bit k % 32
+    of word k // 32 of row q is mask[q, k] (the layout MASK_DENSE reads)."""
+    if not (mask.is_cuda and words.is_cuda):
+        raise ValueError("mask and words must be CUDA tensors")
+    if mask.dim() != 2 or mask.stride(1) != 1 or mask.element_size() != 1:
+        raise ValueError("mask must be a [Sq, Skv] bool/uint8 tensor with "
+                         "contiguous rows")
+    if words.dim() != 2 or words.stride(1) != 1 or words.element_size() != 4:
+        raise ValueError("words must be a [Sq, W] 32-bit tensor with "
+                         "contiguous rows")
     Sq, Skv = mask.shape
-    W = (Skv + 31) // 32
-    pad = torch.zeros((Sq, W * 32), dtype=torch.int64, device=mask.device)
-    pad[:, :Skv] = mask.to(torch.int64)
-    weights = torch.ones(32, dtype=torch.int64, device=mask.device)
-    weights = torch.bitwise_left_shift(weights,
-                                       torch.arange(32, device=mask.device))
-    words = (pad.view(Sq, W, 32) * weights).sum(dim=2)
-    # reinterpret the low 32 bits as int32
-    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words)
-    return words.to(torch.int32).contiguous()
+    if words.shape[0] != Sq:
+        raise ValueError("words must have one row per mask row")
+    _check(_lib.lib().bsm_pack_dense_mask(
+        mask.data_ptr(), mask.stride(0), Sq, Skv, words.data_ptr(),
+        words.stride(0), _stream_handle(stream)))
+
+
+def pack_dense_mask(mask: torch.Tensor, stream=None) -> torch.Tensor:
+    """bsm_pack_dense_mask into a new int32 tensor [Sq, ceil(Skv / 32)]."""
+    Sq, Skv = mask.shape
+    if mask.dtype != torch.bool and mask.dtype != torch.uint8:
+        mask = mask != 0
+    mask = mask.contiguous()
+    words = torch.empty((Sq, (Skv + 31) // 32), dtype=torch.int32,
+                        device=mask.device)
+    bsm_pack_dense_mask(mask, words, stream)
+    return words
 
 
 def splash_attention_bwd(q, k, v, out, lse, dout, *,

@@ -492,6 +492,29 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
   return BSM_OK;
 }
 
+bsm_status bsm_pack_dense_mask(const uint8_t* mask, int64_t mask_row_stride,
+                               int32_t Sq, int32_t Skv, uint32_t* words,
+                               int32_t row_words, void* stream) {
+  g_last_error.clear();
+  if (Sq < 0 || Skv < 0)
+    return fail(BSM_ERR_INVALID_ARG, "Sq and Skv must be >= 0");
+  if (row_words < (static_cast<int64_t>(Skv) + 31) / 32)
+    return fail(BSM_ERR_INVALID_ARG, "row_words must be >= ceil(Skv / 32)");
+  if (mask_row_stride < Skv)
+    return fail(BSM_ERR_INVALID_ARG, "mask_row_stride must be >= Skv");
+  if (static_cast<int64_t>(Sq) * row_words == 0) return BSM_OK;
+  if (mask == nullptr || words == nullptr)
+    return fail(BSM_ERR_INVALID_ARG, "mask and words must be non-NULL");
+  int num_sms = 0;
+  bsm_status s = check_device(&num_sms);
+  if (s != BSM_OK) return s;
+  const cudaError_t e = bsm::launch_pack_dense(
+      mask, mask_row_stride, Sq, Skv, words, row_words, num_sms,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pack_dense launch");
+  return BSM_OK;
+}
+
 size_t bsm_splash_fwd_workspace_bytes(void) { return bsm::kFwdWorkspaceBytes; }
 
 size_t bsm_splash_bwd_workspace_bytes(int32_t B, int32_t H, int32_t Sq,
@@ -704,6 +727,6 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq) {
 
 const char* bsm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t bsm_version(void) { return 300; }
+int32_t bsm_version(void) { return 301; }
 
 }  // extern "C"

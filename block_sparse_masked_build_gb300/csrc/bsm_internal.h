@@ -120,6 +120,9 @@ struct BwdParams {
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_mask_info(const MaskInfoParams& p, cudaStream_t stream);
+cudaError_t launch_pack_dense(const uint8_t* mask, int64_t stride, int32_t Sq,
+                              int32_t Skv, uint32_t* words, int32_t row_words,
+                              int num_sms, cudaStream_t stream);
 // Whether a mask of these sizes is built in one launch.
 bool mask_info_fused(int64_t tables, int64_t nq, int64_t nk);
 int fwd_grid_size(const FwdParams& p, int num_sms);

@@ -577,7 +577,56 @@ __global__ void __launch_bounds__(kMiThreads)
   }
 }
 
+// Bit-packs a boolean mask, one thread per output word: bit i of word w of
+// row q is mask[q][32 w + i] != 0 (zero past Skv and in row padding).  With
+// 16-byte aligned rows a word's 32 bytes are two 16-byte loads, and each
+// 4-byte lane becomes 4 bits through a per-byte compare.
+__global__ void __launch_bounds__(256)
+    pack_dense_kernel(const uint8_t* __restrict__ mask, int64_t stride,
+                      int32_t Sq, int32_t Skv, uint32_t* __restrict__ words,
+                      int32_t row_words, int vec16) {
+  const int64_t total = static_cast<int64_t>(Sq) * row_words;
+  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       w < total; w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t q = w / row_words;
+    const int k0 = static_cast<int>(w - q * row_words) * 32;
+    const uint8_t* row = mask + q * stride;
+    uint32_t bits = 0;
+    if (k0 + 32 <= Skv && vec16) {
+      const uint4* src = reinterpret_cast<const uint4*>(row + k0);
+      const uint4 a = __ldg(src), b = __ldg(src + 1);
+      const uint32_t lanes[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ne = __vcmpne4(lanes[i], 0u);  // 0xff per nonzero byte
+        const uint32_t nib = ((ne >> 7) & 1u) | ((ne >> 14) & 2u) |
+                             ((ne >> 21) & 4u) | ((ne >> 28) & 8u);
+        bits |= nib << (4 * i);
+      }
+    } else {
+      const int n = min(32, Skv - k0);  // <= 0 in the row padding
+      for (int i = 0; i < n; ++i) bits |= (row[k0 + i] != 0 ? 1u : 0u) << i;
+    }
+    words[w] = bits;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_dense(const uint8_t* mask, int64_t stride, int32_t Sq,
+                              int32_t Skv, uint32_t* words, int32_t row_words,
+                              int num_sms, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(Sq) * row_words;
+  if (total == 0) return cudaSuccess;
+  const int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+  const int vec16 = ((reinterpret_cast<uintptr_t>(mask) & 15u) == 0 &&
+                     (stride & 15) == 0) ? 1 : 0;
+  pack_dense_kernel<<<grid, 256, 0, stream>>>(mask, stride, Sq, Skv, words,
+                                              row_words, vec16);
+  return cudaGetLastError();
+}
 
 bool mask_info_fused(int64_t tables, int64_t nq, int64_t nk) {
   return tables * nq < (int64_t{1} << kTicketBits) &&

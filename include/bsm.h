@@ -156,6 +156,20 @@ bsm_status bsm_build_mask_info(const bsm_mask_spec* spec,
                                size_t buffer_bytes, bsm_mask_info* info,
                                void* stream);
 
+/* Bit-pack a boolean mask into the BSM_MASK_DENSE layout (the role of
+ * [HSTU]'s dense mask array, stored as bits): bit k % 32 of word
+ * words[q * row_words + k / 32] is (mask[q * mask_row_stride + k] != 0) for
+ * k < Skv; the rest of each row's words are zero.
+ *   mask             device uint8 [Sq][mask_row_stride] (torch.bool bytes)
+ *   words            device uint32 [Sq][row_words], row_words >=
+ *                    ceil(Skv / 32); pass it as bsm_mask_spec.dense_bits
+ * One kernel launch on `stream`.  Returns BSM_ERR_INVALID_ARG for negative
+ * sizes, row_words or mask_row_stride too small, or a NULL pointer with a
+ * nonempty mask. */
+bsm_status bsm_pack_dense_mask(const uint8_t* mask, int64_t mask_row_stride,
+                               int32_t Sq, int32_t Skv, uint32_t* words,
+                               int32_t row_words, void* stream);
+
 /* Block-sparse masked attention forward ([NOTES] sections 15, 18, 21;
  * [HSTU] _pointwise_splash_attention_fwd_kernel_impl).  For each (batch,
  * head, 128-row query tile) the kernel walks only the KV tiles the mask-info
@@ -319,9 +333,9 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq);
 /* Thread-local text of the last error of this thread ("" if none). */
 const char* bsm_last_error(void);
 
-/* ABI version (major*10000 + minor*100 + patch): 300 = 0.3.0, the
- * backward entry points and bsm_tensor added to 0.2.0's forward, mask spec
- * and mask info. */
+/* ABI version (major*10000 + minor*100 + patch): 301 = 0.3.1, adding
+ * bsm_pack_dense_mask to 0.3.0 (the backward entry points and bsm_tensor
+ * added to 0.2.0's forward, mask spec and mask info). */
 int32_t bsm_version(void);
 
 #ifdef __cplusplus

@@ -42,7 +42,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.bsm_version() == 300 == _lib.ABI_VERSION
+    assert lib.bsm_version() == 301 == _lib.ABI_VERSION
 
 
 def test_library_is_built_for_sm_103a(lib):
@@ -197,17 +197,26 @@ def test_selftest_rejects_out_of_range_limits(lib):
     assert lib.bsm_selftest_wait_timeout(10**12, None) == INVALID
 
 
-def test_torch_dense_packing_matches_layout():
-    # the binding's on-device packer (run here on CPU tensors) produces the
-    # documented layout: bit k % 32 of word k // 32 of row q
-    import numpy as np
+def test_dense_packing_needs_cuda_tensors():
+    # packing runs in the library's kernel only: CPU tensors are refused,
+    # never packed on the host
+    import pytest as _pytest
     import torch
     import block_sparse_masked_build_gb300 as bsm
-    from block_sparse_masked_build_gb300 import workloads as wl
-    m = wl.random_dense_mask(45, 70, 0.5, 16, 31)
-    got = bsm.pack_dense_mask(torch.from_numpy(m)).numpy().view(np.uint32)
-    np.testing.assert_array_equal(got, wl.pack_dense_mask(m))
-    assert got.shape == (45, 3)
+    m = torch.zeros((4, 40), dtype=torch.bool)
+    w = torch.zeros((4, 2), dtype=torch.int32)
+    with _pytest.raises(ValueError):
+        bsm.bsm_pack_dense_mask(m, w)
+
+
+def test_pack_dense_mask_argument_checks(lib):
+    # row_words below ceil(Skv / 32), a row stride below Skv, negative sizes
+    assert lib.bsm_pack_dense_mask(None, 64, 4, 64, None, 1, None) == INVALID
+    assert lib.bsm_pack_dense_mask(None, 32, 4, 64, None, 2, None) == INVALID
+    assert lib.bsm_pack_dense_mask(None, 64, -1, 64, None, 2, None) == INVALID
+    assert lib.bsm_pack_dense_mask(None, 64, 4, 64, None, 2, None) == INVALID
+    # an empty mask is a no-op
+    assert lib.bsm_pack_dense_mask(None, 0, 0, 0, None, 0, None) == 0
 
 
 def test_bwd_workspace_bytes(lib):

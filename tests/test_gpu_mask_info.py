@@ -229,3 +229,56 @@ def test_segment_ranges_and_sorted_flag(sorted_ids):
             hi = np.searchsorted(kv_seg[b], q_seg[b], side="right") - 1
             np.testing.assert_array_equal(got[b, :, 0], lo)
             np.testing.assert_array_equal(got[b, :, 1], hi)
+
+
+# ---- bit-packing of an arbitrary mask (the library's packing kernel)
+
+@pytest.mark.parametrize("Sq,Skv,offset,extra_words,dtype", [
+    (45, 70, 0, 0, "bool"),        # ragged last word, aligned rows
+    (128, 4096, 0, 0, "bool"),     # whole words only, 16-byte loads
+    (33, 97, 3, 5, "bool"),        # unaligned rows (byte loads), row padding
+    (257, 1000, 16, 2, "uint8"),   # nonzero bytes other than 1 count as set
+])
+def test_pack_dense_mask_kernel_layout(Sq, Skv, offset, extra_words, dtype):
+    """bit k % 32 of word k // 32 of row q is mask[q, k]; padding words 0."""
+    m = wl.random_dense_mask(Sq, Skv, 0.5, 16, Sq + Skv)
+    dev = torch.device("cuda")
+    stride = Skv + offset
+    raw = np.zeros(offset + Sq * stride, dtype=np.uint8)
+    vals = m.astype(np.uint8)
+    if dtype == "uint8":  # any nonzero byte is "visible"
+        rng = np.random.default_rng(5)
+        vals = vals * rng.integers(1, 256, size=m.shape, dtype=np.uint8)
+    raw[offset:].reshape(Sq, stride)[:, :Skv] = vals
+    buf = torch.from_numpy(raw).to(dev)
+    if dtype == "bool":
+        buf = buf.view(torch.bool)
+    view = buf[offset:].view(Sq, stride)[:, :Skv]
+    W = -(-Skv // 32) + extra_words
+    words = torch.full((Sq, W), -1, dtype=torch.int32, device=dev)
+    bsm.bsm_pack_dense_mask(view, words)
+    torch.cuda.synchronize()
+    got = words.cpu().numpy().view(np.uint32)
+    np.testing.assert_array_equal(got, wl.pack_dense_mask(m, W))
+
+
+def test_splash_attention_packs_a_dense_mask_on_the_device():
+    """The end-to-end call with a boolean mask: packed by the library's
+    kernel, then the forward against the oracle."""
+    from gpu_helpers import compare_out, compare_lse
+    B, H, Sq, Skv, D = 1, 2, 384, 448, 64
+    g = torch.Generator().manual_seed(77)
+    q = torch.randn(B, H, Sq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, Skv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, Skv, D, generator=g).to(torch.bfloat16)
+    m = wl.random_dense_mask(Sq, Skv, 0.4, 64, 78)
+    dev = torch.device("cuda")
+    out, lse = bsm.splash_attention(
+        q.to(dev), k.to(dev), v.to(dev), mask_flags=bsm.MASK_DENSE,
+        dense_mask=torch.from_numpy(m).to(dev))
+    torch.cuda.synchronize()
+    scale = 1.0 / np.sqrt(D)
+    ref, ref_lse = oracle.softmax_attention(q, k, v, bsm.MASK_DENSE, 0, None,
+                                            None, scale, dense=m)
+    compare_out(out.float().cpu().numpy(), ref, what="dense out")
+    compare_lse(lse.cpu().numpy(), ref_lse, what="dense lse")
