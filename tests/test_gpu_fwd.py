@@ -415,3 +415,22 @@ def test_full_size_grouped_heads_every_row_of_sampled_heads():
             w.window, None, None, w.scale)
         compare_out(out[b:b + 1, h:h + 1].numpy(), ref, what=f"b{b} h{h}")
         compare_lse(lse[b:b + 1, h:h + 1].numpy(), ref_lse, what=f"b{b} h{h}")
+
+
+def test_maximum_sequence_length_local_window():
+    """Sq = Skv = 262144, the longest sequence the kernels take (2048 x 2048
+    mask blocks: the mask-info build takes its three-launch path), under a
+    local window of 1024 keys, two heads; one row of every 256-row work
+    unit is compared with the oracle, at a varying offset in the unit."""
+    B, H, S, D = 1, 2, 262144, 64
+    q, k, v = _qkv(B, H, H, S, S, D, 4242)
+    scale = 1.0 / math.sqrt(D)
+    out, lse, _ = run_gpu(q, k, v, L, 1024, None, None, scale, SM)
+    units = S // 256
+    rows = [(0, u % H, u * 256 + (u * 37) % 256) for u in range(units)]
+    ref, ref_lse = oracle.softmax_attention(q, k, v, L, 1024, None, None,
+                                            scale, rows=rows)
+    got = np.stack([out[b, h, r].float().numpy() for b, h, r in rows])
+    got_lse = np.array([lse[b, h, r].item() for b, h, r in rows])
+    compare_out(got, ref, what="max-length out")
+    compare_lse(got_lse, ref_lse, what="max-length lse")

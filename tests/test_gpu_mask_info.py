@@ -179,11 +179,14 @@ def test_super_order_absent_above_limit():
     assert got["super_order"] is None and got["num_super"] == 1024
 
 
-def test_large_causal_mask_lists_closed_form():
-    # 1024 x 1024 block cells (more than 2^14: the lists are written by the
-    # separate per-row compaction): causal classes are 2 below the diagonal,
-    # 1 on it, 0 above; each row's list is its nonzero blocks in order
-    S, b = 65536, 64
+@pytest.mark.parametrize("S,b", [
+    (65536, 64),    # 2^20 block cells: the one-launch build's largest mask
+    (131072, 64),   # 2^22 cells: classify, a one-CTA scan, a compaction
+    (262144, 128),  # the longest sequence the kernels take
+])
+def test_large_causal_mask_lists_closed_form(S, b):
+    # causal classes are 2 below the diagonal, 1 on it, 0 above; each row's
+    # list is its nonzero blocks in order
     got = _gpu_info(1, 0, None, None, 1, S, S, b, b)
     n = S // b
     i = np.arange(n)[:, None]
@@ -192,7 +195,7 @@ def test_large_causal_mask_lists_closed_form():
     np.testing.assert_array_equal(got["block_mask"].reshape(n, n), want)
     rp = got["row_ptr"]
     np.testing.assert_array_equal(np.diff(rp), np.arange(1, n + 1))
-    for r in (0, 1, 517, n - 1):
+    for r in (0, 1, 517, n // 2 + 3, n - 1):
         np.testing.assert_array_equal(got["kv_idx"][rp[r]:rp[r + 1]],
                                       np.arange(r + 1))
         np.testing.assert_array_equal(got["kv_cls"][rp[r]:rp[r + 1]],
