@@ -38,7 +38,7 @@
 namespace bsm {
 namespace {
 
-constexpr int kMiThreads = 256;
+constexpr int kMiThreads = 512;
 constexpr int kStagedKeys = 32768;  // kv ids staged in shared memory (128 KB)
 // Masks of at most this many block cells (and fewer than 2^24 rows) are
 // built in one launch.
@@ -202,6 +202,18 @@ __device__ __forceinline__ void finish_tables(const MaskInfoParams& p,
     keys[i] = key;
   }
   __syncthreads();
+  if (pairs <= static_cast<int>(blockDim.x)) {
+    // few pairs: each key's rank is the number of smaller keys (the index
+    // bits make the keys of distinct pairs distinct); one pass, no barriers
+    if (static_cast<int>(threadIdx.x) < pairs) {
+      const uint32_t mine = keys[threadIdx.x];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < pairs; ++j) rank += keys[j] < mine ? 1 : 0;
+      p.super_order[rank] = static_cast<int32_t>(threadIdx.x);
+    }
+    return;
+  }
   // bitonic sort of keys[0..n2)
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
