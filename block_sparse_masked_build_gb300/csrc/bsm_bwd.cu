@@ -70,8 +70,11 @@ static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 struct BwdBars {
   uint64_t f_full;
   uint64_t t_full[2], t_empty[2];
-  uint64_t s_full, dp_full, p_ready, acc_done, mma_done;
-  uint64_t h0_read;  // the first column half has read S and dP
+  uint64_t s_full, dp_full, acc_done, mma_done;
+  // elementwise -> MMA: P stored (dK/dV) or S read (dQ); dS stored
+  uint64_t p_ready, ds_ready;
+  // the first column half has read S, and dP
+  uint64_t h0_s, h0_dp;
   uint32_t tmem_base;
   int abort;
   int n_list;
@@ -306,34 +309,49 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
       sdesc_sw128(smem_u32(smem + C::kOffT), kTileN * 128, 1024);
   const uint32_t t_s = tmem, t_dp = tmem + 128;
   const uint32_t t_acc0 = tmem + 256, t_acc1 = tmem + 384;
+  // S = F0 T0^T and dP = F1 T1^T of step `it` from ring slot it & 1
+  auto issue_s = [&](int it) {
+    const uint64_t t0 = db + (it & 1) * 2 * kTileUnits;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+      mma_ss(t_s, da + off, t0 + off, idesc_s, k > 0 ? 1u : 0u);
+    }
+    mma_commit(&bars->s_full);
+  };
+  auto issue_dp = [&](int it) {
+    const uint64_t t1 = db + (it & 1) * 2 * kTileUnits + kTileUnits;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+      mma_ss(t_dp, da + kTileUnits + off, t1 + off, idesc_s,
+             k > 0 ? 1u : 0u);
+    }
+    mma_commit(&bars->dp_full);
+  };
+  // Per step: once P is stored (dK/dV) or S has been read (dQ), dV += P T1
+  // and the next step's S go in; once dS is stored, dK += dS T0 (dQ += dS
+  // T0) and the next step's dP.  The next S and dP overwrite the TMEM
+  // columns that P and dS occupy; tcgen05 MMAs of one thread run in issue
+  // order, so they come after the products that read them, and the
+  // elementwise warps work on the next S while dS, dK and dP are in flight.
   bool ok = bwarp_wait(&bars->f_full, 0, abort_flag, p.timeout_ns);
   if (!ok && leader) record_bwd_timeout(kRoleBMma, 0);
-  for (int it = 0; ok && it < n_iter; ++it) {
-    const int s = it & 1;
-    ok = bwarp_wait(&bars->t_full[s], (it >> 1) & 1, abort_flag, p.timeout_ns);
-    if (!ok) {
-      if (leader) record_bwd_timeout(kRoleBMma, 1);
-      break;
-    }
-    const uint64_t t0 = db + s * 2 * kTileUnits;  // T0 (K-major)
-    const uint64_t t1 = t0 + kTileUnits;          // T1
-    if (leader) {
+  if (ok && n_iter > 0) {
+    ok = bwarp_wait(&bars->t_full[0], 0, abort_flag, p.timeout_ns);
+    if (!ok && leader) record_bwd_timeout(kRoleBMma, 1);
+    if (ok && leader) {
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
-        mma_ss(t_s, da + off, t0 + off, idesc_s, k > 0 ? 1u : 0u);
-      }
-      mma_commit(&bars->s_full);
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
-        mma_ss(t_dp, da + kTileUnits + off, t1 + off, idesc_s,
-               k > 0 ? 1u : 0u);
-      }
-      mma_commit(&bars->dp_full);
+      issue_s(0);
+      issue_dp(0);
     }
     __syncwarp();
+  }
+  for (int it = 0; ok && it < n_iter; ++it) {
+    const int s = it & 1;
+    const uint64_t m0 = dbm + s * 2 * kTileUnits;  // T0 read MN-major
+    const uint64_t m1 = m0 + kTileUnits;           // T1 read MN-major
+    const uint32_t first = it == 0 ? 0u : 1u;
     ok = bwarp_wait(&bars->p_ready, it & 1, abort_flag, p.timeout_ns);
     if (!ok) {
       if (leader) record_bwd_timeout(kRoleBMma, 2);
@@ -341,9 +359,6 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
     }
     if (leader) {
       tc_fence_after();
-      const uint64_t m0 = dbm + s * 2 * kTileUnits;  // T0 read MN-major
-      const uint64_t m1 = m0 + kTileUnits;           // T1 read MN-major
-      const uint32_t first = it == 0 ? 0u : 1u;
       // bf16 A from TMEM: rows 16kk..16kk+15 of the K dimension in columns
       // 8kk..8kk+7
       if (DKDV) {
@@ -351,17 +366,37 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
         for (int kk = 0; kk < kTileN / 16; ++kk)  // dV += P T1
           mma_ts(t_acc0, t_s + kk * 8, m1 + kk * (16 * 128 / 16), idesc_acc,
                  (kk > 0 || first) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // dK += dS T0
-          mma_ts(t_acc1, t_dp + kk * 8, m0 + kk * (16 * 128 / 16), idesc_acc,
-                 (kk > 0 || first) ? 1u : 0u);
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // dQ += dS T0
-          mma_ts(t_acc0, t_dp + kk * 8, m0 + kk * (16 * 128 / 16), idesc_acc,
-                 (kk > 0 || first) ? 1u : 0u);
       }
+    }
+    __syncwarp();
+    const bool more = it + 1 < n_iter;
+    if (more) {
+      ok = bwarp_wait(&bars->t_full[(it + 1) & 1], ((it + 1) >> 1) & 1,
+                      abort_flag, p.timeout_ns);
+      if (!ok) {
+        if (leader) record_bwd_timeout(kRoleBMma, 1);
+        break;
+      }
+      if (leader) {
+        tc_fence_after();
+        issue_s(it + 1);
+      }
+      __syncwarp();
+    }
+    ok = bwarp_wait(&bars->ds_ready, it & 1, abort_flag, p.timeout_ns);
+    if (!ok) {
+      if (leader) record_bwd_timeout(kRoleBMma, 4);
+      break;
+    }
+    if (leader) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)  // dK (or dQ) += dS T0
+        mma_ts(DKDV ? t_acc1 : t_acc0, t_dp + kk * 8,
+               m0 + kk * (16 * 128 / 16), idesc_acc,
+               (kk > 0 || first) ? 1u : 0u);
       mma_commit(&bars->t_empty[s]);
+      if (more) issue_dp(it + 1);
     }
     __syncwarp();
   }
@@ -416,18 +451,15 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
     const int tile = list[e] >> 2, cls = list[e] & 3;
     const int head = DKDV ? hq_or_hkv * G + it / n_list : hq_or_hkv;
     const int col0 = tile * kTileM + half * 64;  // first column of the half
-    ok = bwarp_wait(&bars->s_full, it & 1, abort_flag, p.timeout_ns) &&
-         bwarp_wait(&bars->dp_full, it & 1, abort_flag, p.timeout_ns);
+    ok = bwarp_wait(&bars->s_full, it & 1, abort_flag, p.timeout_ns);
     if (!ok) {
       record_bwd_timeout(kRoleBElem, 0);
       break;
     }
     tc_fence_after();
-    uint32_t sraw[64], dpraw[64];
+    uint32_t sraw[64];
     tmem_ld32(t_s + half * 64, sraw);
     tmem_ld32(t_s + half * 64 + 32, sraw + 32);
-    tmem_ld32(t_dp + half * 64, dpraw);
-    tmem_ld32(t_dp + half * 64 + 32, dpraw + 32);
     // per-column statistics and visibility of the half's 64 columns
     float lse2_c[2] = {0.f, 0.f}, delta_c[2] = {0.f, 0.f};
     uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
@@ -442,53 +474,96 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
       if (cls == 1) vis[c] = chunk_visible<DKDV>(p, b, row, row_seg, col0 + c * 32);
     }
     tmem_ld_wait();
-    if (half == 0) {
-      tc_fence_before();
-      mbar_arrive(&bars->h0_read);
-    }
-    uint32_t pw[32], dsw[32];
+    tc_fence_before();
+    if (!DKDV) mbar_arrive(&bars->p_ready);  // S read: the next S may go in
+    else if (half == 0) mbar_arrive(&bars->h0_s);
+    // P, and the per-element factor dS needs: softmax dS = P (dP - D_q),
+    // pointwise dS = dP sig (1 + x (1 - sig)) / Sq
+    float f[64];
+    uint32_t pw[32];
 #pragma unroll
     for (int j = 0; j < 64; j += 2) {
-      float pv[2], dsv[2];
+      float pv[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = (j + u) >> 5, jj = (j + u) & 31;
         const float sv = __uint_as_float(sraw[j + u]);
-        const float dpv = __uint_as_float(dpraw[j + u]);
         const bool v = (vis[c] >> jj) & 1u;
         if (SCORE == BSM_SCORE_SOFTMAX) {
           const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c[c], jj)
                                 : lse2_row;
-          const float dl = DKDV ? __shfl_sync(0xffffffffu, delta_c[c], jj)
-                                : delta_row;
           const float pr = v ? ex2_approx(fmaf(sv, p.scale_log2, -l2)) : 0.f;
           pv[u] = pr;
-          dsv[u] = pr * (dpv - dl);
+          f[j + u] = pr;
         } else {
           const float x = sv * p.scale;
           const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
           pv[u] = v ? x * sig * p.inv_sq : 0.f;
-          dsv[u] = v ? dpv * sig * fmaf(x, 1.f - sig, 1.f) * p.inv_sq : 0.f;
+          f[j + u] = v ? sig * fmaf(x, 1.f - sig, 1.f) * p.inv_sq : 0.f;
         }
       }
       pw[j / 2] = pack_bf16x2(pv[0], pv[1]);
+    }
+    if (DKDV) {
+      // P over S's columns: the half's 64 columns pack into columns
+      // 32 * half .. 32 * half + 31; [32, 64) are the first half's S
+      if (half == 1) {
+        if (!bwarp_wait(&bars->h0_s, it & 1, abort_flag, p.timeout_ns)) {
+          record_bwd_timeout(kRoleBElem, 2);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(t_s + half * 32, pw);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+    }
+    ok = bwarp_wait(&bars->dp_full, it & 1, abort_flag, p.timeout_ns);
+    if (!ok) {
+      record_bwd_timeout(kRoleBElem, 3);
+      break;
+    }
+    tc_fence_after();
+    uint32_t dpraw[64];
+    tmem_ld32(t_dp + half * 64, dpraw);
+    tmem_ld32(t_dp + half * 64 + 32, dpraw + 32);
+    tmem_ld_wait();
+    if (half == 0) {
+      tc_fence_before();
+      mbar_arrive(&bars->h0_dp);
+    }
+    uint32_t dsw[32];
+#pragma unroll
+    for (int j = 0; j < 64; j += 2) {
+      float dsv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float dpv = __uint_as_float(dpraw[j + u]);
+        if (SCORE == BSM_SCORE_SOFTMAX) {
+          const int c = (j + u) >> 5, jj = (j + u) & 31;
+          const float dl = DKDV ? __shfl_sync(0xffffffffu, delta_c[c], jj)
+                                : delta_row;
+          dsv[u] = f[j + u] * (dpv - dl);
+        } else {
+          dsv[u] = dpv * f[j + u];
+        }
+      }
       dsw[j / 2] = pack_bf16x2(dsv[0], dsv[1]);
     }
-    if (half == 1) {  // columns [32, 64) are the first half's input
-      if (!bwarp_wait(&bars->h0_read, it & 1, abort_flag, p.timeout_ns)) {
+    if (half == 1) {  // columns [32, 64) of dP are the first half's input
+      if (!bwarp_wait(&bars->h0_dp, it & 1, abort_flag, p.timeout_ns)) {
         record_bwd_timeout(kRoleBElem, 2);
         ok = false;
         break;
       }
       tc_fence_after();
     }
-    // P over S's columns, dS over dP's: the half's 64 columns pack into
-    // columns 32 * half .. 32 * half + 31
-    if (DKDV) tmem_st32(t_s + half * 32, pw);
     tmem_st32(t_dp + half * 32, dsw);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&bars->p_ready);
+    mbar_arrive(&bars->ds_ready);
   }
   if (!ok) return;
   // ---- results: dK/dV rows (keys) or dQ rows, bf16; dK and dQ scaled;
@@ -573,7 +648,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 256);
-    mbar_init(&bars->h0_read, 128);
+    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->h0_s, 128);
+    mbar_init(&bars->h0_dp, 128);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
