@@ -52,6 +52,7 @@ __device__ int g_bwd_error[4];
 namespace {
 
 constexpr int kBwdThreads = 320;  // warps 0-1 roles, 2-9 elementwise
+constexpr int kBwdBand = 16;      // tiles per band of the causal block order
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr int kRoleBLoad = 11, kRoleBMma = 12, kRoleBElem = 13;
 
@@ -633,10 +634,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + C::kOffList);
   const int warp = threadIdx.x / 32;
   // grid: (tile, head, batch); dK/dV: key tile and K/V head; dQ: query tile
-  // and query head
-  const int fixed_tile = blockIdx.x;
-  const int head = blockIdx.y;
-  const int b = blockIdx.z;
+  // and query head.  Blocks start in linear order.  Under a causal mask
+  // (without a window) a walk is longest for the first key tiles (dK/dV)
+  // and the last query tiles (dQ), so the linear index is dealt out in
+  // bands of kBwdBand tiles, longest band first, every (head, batch) of a
+  // band before the next band: long walks start early, and the CTAs in
+  // flight still share a few heads' tiles in L2.
+  int fixed_tile = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
+  if ((p.flags & BSM_MASK_CAUSAL) &&
+      !(p.flags & (BSM_MASK_LOCAL | BSM_MASK_BAND))) {
+    const int X = gridDim.x, G = gridDim.y * gridDim.z;
+    const int lin = blockIdx.x + X * (blockIdx.y + gridDim.y * blockIdx.z);
+    const int band = lin / (kBwdBand * G);
+    const int width = min(kBwdBand, X - band * kBwdBand);
+    const int within = lin - band * kBwdBand * G;
+    const int g = within / width, k = within - g * width;
+    const int rank = band * kBwdBand + k;  // 0 = the longest walk
+    fixed_tile = DKDV ? rank : X - 1 - rank;
+    head = g % gridDim.y;
+    b = g / gridDim.y;
+  }
   const int table = (p.flags & BSM_MASK_SEGMENT) ? b : 0;
 
   if (threadIdx.x == 0) {
