@@ -708,28 +708,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kBwdTmemCols);
 }
 
-// D_q = sum_d dO[q, d] * out[q, d], one warp per (batch, head, row).
+// D_q = sum_d dO[q, d] * out[q, d]: D / 8 threads per (batch, head, row),
+// each with one 16-byte load of out and of dO (rows and strides are 16-byte
+// aligned), a warp covering 32 / (D / 8) rows per pass of a grid-stride
+// loop.
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const BwdParams p) {
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x +
-                      threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
+  const int gs = p.D / 8;  // threads per row: 16 (D = 128) or 8 (D = 64)
+  const int lane = threadIdx.x % 32, sub = lane % gs;
+  const int rpw = 32 / gs;  // rows per warp and pass
   const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
-  if (gw >= rows) return;
-  const int q = static_cast<int>(gw % p.Sq);
-  const int64_t bh = gw / p.Sq;
-  const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
-  const uint16_t* o = p.out + b * p.o_sb + h * p.o_sh + q * p.o_ss;
-  const uint16_t* d = p.dout + b * p.do_sb + h * p.do_sh + q * p.do_ss;
-  float acc = 0.f;
-  for (int c = lane * 2; c < p.D; c += 64) {
-    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o + c);
-    const uint32_t dv = *reinterpret_cast<const uint32_t*>(d + c);
-    acc = fmaf(__uint_as_float(ov << 16), __uint_as_float(dv << 16), acc);
-    acc = fmaf(__uint_as_float(ov & 0xffff0000u),
-               __uint_as_float(dv & 0xffff0000u), acc);
+  const int64_t warp0 =
+      (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+#pragma unroll 2
+  for (int64_t base = warp0 * rpw; base < rows; base += nwarps * rpw) {
+    const int64_t r = base + lane / gs;
+    float acc = 0.f;
+    if (r < rows) {
+      const int q = static_cast<int>(r % p.Sq);
+      const int64_t bh = r / p.Sq;
+      const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
+      const uint4 ov = __ldg(reinterpret_cast<const uint4*>(
+          p.out + b * p.o_sb + h * p.o_sh + q * p.o_ss + sub * 8));
+      const uint4 dv = __ldg(reinterpret_cast<const uint4*>(
+          p.dout + b * p.do_sb + h * p.do_sh + q * p.do_ss + sub * 8));
+      const uint32_t o4[4] = {ov.x, ov.y, ov.z, ov.w};
+      const uint32_t d4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(o4[i] << 16), __uint_as_float(d4[i] << 16),
+                   acc);
+        acc = fmaf(__uint_as_float(o4[i] & 0xffff0000u),
+                   __uint_as_float(d4[i] & 0xffff0000u), acc);
+      }
+    }
+    for (int s = gs / 2; s > 0; s >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (r < rows && sub == 0) p.delta[r] = acc;
   }
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) p.delta[gw] = acc;
 }
 
 template <int D, int SCORE, bool DKDV>
@@ -767,7 +783,12 @@ cudaError_t launch_splash_bwd(const BwdParams& p, const CUtensorMap& tq,
   if (p.score == BSM_SCORE_SOFTMAX) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
     if (rows > 0) {
-      bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256,
+      int dev = 0, sms = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      const int64_t need = (rows * (p.D / 8) + 255) / 256;
+      const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
+      bwd_delta_kernel<<<static_cast<unsigned>(need < cap ? need : cap), 256,
                          0, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
