@@ -446,12 +446,34 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
     lse2_row = p.lse[i] * kLog2e;
     delta_row = p.delta[i];
   }
+  // dK/dV softmax: the lse (log2 units) and D_q of the step's query
+  // columns, loaded a step ahead so that their latency hides behind the
+  // current step
+  auto load_stats = [&](int it, float (&l2)[2], float (&dl)[2]) {
+    const int tile = list[it % n_list] >> 2;
+    const int hd = hq_or_hkv * G + it / n_list;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int qc = tile * kTileM + half * 64 + c * 32 + lane;
+      l2[c] = 0.f;
+      dl[c] = 0.f;
+      if (qc < p.Sq) {
+        const int64_t i = (static_cast<int64_t>(b) * p.H + hd) * p.Sq + qc;
+        l2[c] = p.lse[i] * kLog2e;
+        dl[c] = p.delta[i];
+      }
+    }
+  };
+  constexpr bool kStats = DKDV && SCORE == BSM_SCORE_SOFTMAX;
+  float lse2_n[2] = {0.f, 0.f}, delta_n[2] = {0.f, 0.f};
+  if (kStats && n_iter > 0) load_stats(0, lse2_n, delta_n);
   bool ok = true;
   for (int it = 0; it < n_iter; ++it) {
     const int e = it % n_list;
     const int tile = list[e] >> 2, cls = list[e] & 3;
-    const int head = DKDV ? hq_or_hkv * G + it / n_list : hq_or_hkv;
     const int col0 = tile * kTileM + half * 64;  // first column of the half
+    float lse2_c[2] = {lse2_n[0], lse2_n[1]}, delta_c[2] = {delta_n[0], delta_n[1]};
+    if (kStats && it + 1 < n_iter) load_stats(it + 1, lse2_n, delta_n);
     ok = bwarp_wait(&bars->s_full, it & 1, abort_flag, p.timeout_ns);
     if (!ok) {
       record_bwd_timeout(kRoleBElem, 0);
@@ -461,19 +483,11 @@ __device__ __forceinline__ void bwd_elem_role(const BwdParams& p,
     uint32_t sraw[64];
     tmem_ld32(t_s + half * 64, sraw);
     tmem_ld32(t_s + half * 64 + 32, sraw + 32);
-    // per-column statistics and visibility of the half's 64 columns
-    float lse2_c[2] = {0.f, 0.f}, delta_c[2] = {0.f, 0.f};
+    // visibility of the half's 64 columns
     uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int qc = col0 + c * 32 + lane;
-      if (DKDV && SCORE == BSM_SCORE_SOFTMAX && qc < p.Sq) {
-        const int64_t i = (static_cast<int64_t>(b) * p.H + head) * p.Sq + qc;
-        lse2_c[c] = p.lse[i] * kLog2e;
-        delta_c[c] = p.delta[i];
-      }
+    for (int c = 0; c < 2; ++c)
       if (cls == 1) vis[c] = chunk_visible<DKDV>(p, b, row, row_seg, col0 + c * 32);
-    }
     tmem_ld_wait();
     tc_fence_before();
     if (!DKDV) mbar_arrive(&bars->p_ready);  // S read: the next S may go in
