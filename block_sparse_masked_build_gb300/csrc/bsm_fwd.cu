@@ -1012,6 +1012,715 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decoupled query tiles, for packed sequences (segment ids).  There the
+// units are short and the two query tiles of a unit often need different KV
+// tiles, so the lockstep pipeline above spends much of its time at unit
+// boundaries and on entries one tile skips.  Here the two 128-row query
+// tiles of an SM are two independent pipelines: each takes its own work
+// units (one query tile of one (batch, head)), builds its own KV-tile list,
+// and has its own Q buffer and two-slot K/V ring, so one pipeline's unit
+// boundary overlaps the other's work on the tensor core.  K/V tiles are not
+// shared between the tiles (L2 carries the reuse).
+//
+// Warp roles (384 threads, three warpgroups, registers split as above):
+// warps 0/1 take pipeline 0/1's units, build their lists and load their
+// tiles; warps 2/3 issue its MMAs (warp 2 also owns the TMEM); warps 4-7
+// and 8-11 are the score warpgroups of pipeline 0 and 1.  TMEM as above:
+// S_t/P_t at [128 t, +128), O_t at [256 + 128 t, +128).  Head dim 128,
+// softmax or pointwise.
+constexpr int kDtThreads = 384;
+constexpr int kDtTile = kTileM * 128 * 2;  // one 128 x 128 bf16 tile
+constexpr int kDtOffQ = 0;                 // Q of pipeline t at t tiles
+constexpr int kDtOffKV = 2 * kDtTile;      // ring slot s of pipeline t
+constexpr int kDtOffBar = kDtOffKV + 4 * kDtTile;
+constexpr int kDtSmemBytes = kDtOffBar + 1024 + 1024;
+static_assert(kDtSmemBytes <= 232448, "shared memory budget");
+
+struct DtMeta {
+  int n;     // entries (KV tiles) of the unit
+  int unit;  // -1: no unit left
+  int b, h;  // batch row and head
+  int qt;    // 128-row query tile
+};
+
+struct DtBars {
+  uint64_t list_full[2][kListBufs], list_free[2][kListBufs];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[2][2], kv_empty[2][2];  // [pipeline][slot]: K, V
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2], mma_done[2];
+  uint32_t tmem_base;
+  int abort;
+  uint32_t trace_n[6];
+  DtMeta meta[2][kListBufs];
+};
+static_assert(sizeof(DtBars) <= 1024, "barrier block");
+
+// Optional event trace, in the layout of `trace` above; the six recording
+// threads are: loader 0, MMA 0, score 0, score 1, loader 1, MMA 1.
+template <bool TRACE>
+__device__ __forceinline__ void dt_trace(const FwdParams& p, DtBars* bars,
+                                         uint32_t role, uint32_t ev,
+                                         uint32_t tile, uint32_t entry,
+                                         uint32_t unit) {
+  if (!TRACE) return;
+  const uint32_t slot = role == kRoleScore ? 2 + tile
+                        : role == kRoleMma   ? (tile == 0 ? 1 : 5)
+                                             : (tile == 0 ? 0 : 4);
+  const uint32_t per = p.trace_cap / 6;
+  const uint32_t i = bars->trace_n[slot]++;
+  if (i < per) {
+    TraceRec* r = reinterpret_cast<TraceRec*>(p.trace) +
+                  static_cast<size_t>(blockIdx.x) * (p.trace_cap + 2) + 2 +
+                  slot * per + i;
+    r->t = globaltimer_ns();
+    r->a = (role << 28) | (ev << 24) | (tile << 20) | (entry & 0xFFFFFu);
+    r->b = unit;
+  }
+}
+
+// Takes pipeline t's next unit from the counter and writes its KV-tile
+// list (uint16: tile << 2 | class) into buffer ui % kListBufs (whole warp);
+// unit -1 when none is left.  Units are numbered two per 256-row unit of
+// the lockstep kernel's order (its two query tiles), longest first.
+template <bool TRACE>
+__device__ __forceinline__ bool dt_build_list(const FwdParams& p, DtBars* bars,
+                                              uint16_t* lists, const int t,
+                                              const int ui) {
+  const int lane = threadIdx.x % 32;
+  volatile int* abort_flag = &bars->abort;
+  const int n_units = 2 * p.num_units;
+  {
+    const int buf = ui % kListBufs;
+    if (!warp_wait(&bars->list_free[t][buf], ((ui / kListBufs) & 1) ^ 1,
+                   abort_flag, p.timeout_ns)) {
+      if (lane == 0) record_timeout(kRoleList, 0);
+      return false;
+    }
+    int unit = 0;
+    if (lane == 0) unit = atomicAdd(p.unit_counter, 1);
+    unit = __shfl_sync(0xffffffffu, unit, 0);
+    DtMeta& mt = bars->meta[t][buf];
+    if (unit >= n_units) {
+      if (lane == 0) {
+        mt.unit = -1;
+        mt.n = 0;
+        mbar_arrive(&bars->list_full[t][buf]);
+      }
+      __syncwarp();
+      return true;
+    }
+    const UnitCoord uc = decode_unit(p, unit >> 1);
+    const int qt = uc.st * 2 + (unit & 1);
+    const int table = (p.flags & BSM_MASK_SEGMENT) ? uc.b : 0;
+    uint16_t* list = lists + buf * kMaxKvTiles;
+    int n = 0;
+    for (int base = 0; base < p.n_kvtiles; base += 64) {
+      int c[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int jt = base + 32 * h + lane;
+        c[h] = jt < p.n_kvtiles ? tile_class(p, table, qt * kTileM, jt) : 0;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int jt = base + 32 * h + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, c[h] != 0);
+        if (c[h]) list[n + __popc(m & ((1u << lane) - 1u))] =
+            static_cast<uint16_t>((jt << 2) | c[h]);
+        n += __popc(m);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mt.n = n;
+      mt.unit = unit;
+      mt.b = uc.b;
+      mt.h = uc.h;
+      mt.qt = qt;
+      dt_trace<TRACE>(p, bars, kRoleList, kEvListBuilt, t, n, unit);
+      mbar_arrive(&bars->list_full[t][buf]);
+    }
+    __syncwarp();
+  }
+  return true;
+}
+
+// Pipeline t's loader: builds the next unit's list, then loads its Q and
+// the K and V of every entry through the pipeline's two slots (K in slot
+// 0, V in slot 1).  The next list is built once this unit's last loads are
+// issued, i.e. while the unit's last entries still run (building it after
+// the first entry's loads measured slower).
+template <bool TRACE>
+__device__ __forceinline__ void dt_load_role(const FwdParams& p,
+                                             const CUtensorMap* tq,
+                                             const CUtensorMap* tk,
+                                             const CUtensorMap* tv,
+                                             uint8_t* smem, DtBars* bars,
+                                             uint16_t* lists, const int t) {
+  const int lane = threadIdx.x % 32;
+  volatile int* abort_flag = &bars->abort;
+  const uint64_t pol_q = l2_policy_evict_first();
+  const uint64_t pol_kv = l2_policy_evict_last();
+  uint32_t kv_it = 0, q_it = 0;
+  bool ok = true;
+  for (int ui = 0; ok; ++ui) {
+    const int buf = ui % kListBufs;
+    ok = dt_build_list<TRACE>(p, bars, lists, t, ui);
+    if (!ok) break;
+    const DtMeta mt = bars->meta[t][buf];
+    if (mt.unit < 0) break;
+    const uint16_t* list = lists + buf * kMaxKvTiles;
+    if (mt.n > 0) {
+      ok = warp_wait(&bars->q_empty[t], (q_it & 1) ^ 1, abort_flag,
+                     p.timeout_ns);
+      if (!ok) {
+        if (lane == 0) record_timeout(kRoleLoad, 1);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[t], kDtTile);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_4d(tq, &bars->q_full[t],
+                      smem + kDtOffQ + t * kDtTile + kb * kTileM * 128,
+                      kb * 64, mt.qt * kTileM, mt.h, mt.b, pol_q);
+        dt_trace<TRACE>(p, bars, kRoleLoad, kEvQIssued, t, 0, mt.unit);
+      }
+      ++q_it;
+    }
+    const int hkv = mt.h / (p.H / p.Hkv);
+    for (int e = 0; ok && e < mt.n; ++e) {
+      const int jt = static_cast<int>(list[e] >> 2);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        if (!ok) break;
+        const uint32_t ph = (kv_it >> 1) & 1;
+        ok = warp_wait(&bars->kv_empty[t][which], ph ^ 1, abort_flag,
+                       p.timeout_ns);
+        if (!ok) {
+          if (lane == 0) record_timeout(kRoleLoad, 2);
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->kv_full[t][which], kDtTile);
+          uint8_t* dst = smem + kDtOffKV + (2 * t + which) * kDtTile;
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(which == 0 ? tk : tv, &bars->kv_full[t][which],
+                        dst + kb * kTileN * 128, kb * 64, jt * kTileN, hkv,
+                        mt.b, pol_kv);
+          dt_trace<TRACE>(p, bars, kRoleLoad, kEvTmaIssued, t, e * 2 + which, mt.unit);
+        }
+        ++kv_it;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->list_free[t][buf]);
+  }
+  // Drain the loads already issued (each slot received kv_it / 2 loads).
+  if (lane == 0) {
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t n = (kv_it + 1 - s) >> 1;  // loads slot s received
+      if (n > 0 && !mbar_wait_drain(&bars->kv_full[t][s], (n - 1) & 1,
+                                    p.timeout_ns) && ok)
+        record_timeout(kRoleLoad, 3);
+    }
+    if (q_it > 0 && !mbar_wait_drain(&bars->q_full[t], (q_it - 1) & 1,
+                                     p.timeout_ns) && ok)
+      record_timeout(kRoleLoad, 4);
+  }
+  __syncwarp();
+}
+
+// Pipeline t's MMA issuer (lane 0; the warp waits together): S(e) = Q K(e)^T,
+// then O += P(e) V(e) and S(e + 1) right behind it (tcgen05 MMAs of one
+// thread run in issue order, so S(e + 1) overwrites the columns P(e) V read
+// only after that product).  The K slot is released once the S that read it
+// completed, the V slot once the P.V did.
+template <int SCORE, bool TRACE>
+__device__ __forceinline__ void dt_mma_role(const FwdParams& p, uint8_t* smem,
+                                            DtBars* bars, uint32_t tmem,
+                                            const int t) {
+  const bool leader = (threadIdx.x % 32) == 0;
+  volatile int* abort_flag = &bars->abort;
+  constexpr uint32_t idesc_s = idesc_bf16_f32(kTileM, kTileN, false);
+  constexpr uint32_t idesc_o = idesc_bf16_f32(kTileM, 128, true);
+  const uint64_t dq =
+      sdesc_sw128(smem_u32(smem + kDtOffQ + t * kDtTile), 16, 1024);
+  const uint64_t dk =
+      sdesc_sw128(smem_u32(smem + kDtOffKV + (2 * t) * kDtTile), 16, 1024);
+  const uint64_t dv = sdesc_sw128(
+      smem_u32(smem + kDtOffKV + (2 * t + 1) * kDtTile), kTileN * 128, 1024);
+  const uint32_t s_acc = tmem + t * 128;
+  const uint32_t o_acc = tmem + 256 + t * 128;
+  uint32_t k_it = 0, v_it = 0, q_it = 0, s_cnt = 0;
+  bool ok = true;
+  auto fail = [&](int where) {
+    if (leader) record_timeout(kRoleMma, where);
+  };
+  auto issue_s = [&]() {
+#pragma unroll
+    for (int k = 0; k < 128 / 16; ++k) {
+      const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
+      mma_ss(s_acc, dq + off, dk + off, idesc_s, k > 0 ? 1u : 0u);
+    }
+    mma_commit(&bars->s_full[t]);
+  };
+  for (int ui = 0; ok; ++ui) {
+    const int buf = ui % kListBufs;
+    ok = warp_wait(&bars->list_full[t][buf], (ui / kListBufs) & 1, abort_flag,
+                   p.timeout_ns);
+    if (!ok) {
+      fail(0);
+      break;
+    }
+    const DtMeta mt = bars->meta[t][buf];
+    if (mt.unit < 0) break;
+    const int n = mt.n;
+    if (n > 0) {
+      ok = warp_wait(&bars->q_full[t], q_it & 1, abort_flag, p.timeout_ns) &&
+           warp_wait(&bars->kv_full[t][0], k_it & 1, abort_flag, p.timeout_ns);
+      if (!ok) {
+        fail(1);
+        break;
+      }
+      ++q_it;
+      ++k_it;
+      if (leader) {
+        tc_fence_after();
+        issue_s();
+        dt_trace<TRACE>(p, bars, kRoleMma, kEvSIssued, t, 0, mt.unit);
+        if (n == 1) mma_commit(&bars->q_empty[t]);
+        mma_commit(&bars->kv_empty[t][0]);
+      }
+      ++s_cnt;
+      __syncwarp();
+    }
+    for (int e = 0; ok && e < n; ++e) {
+      ok = warp_wait(&bars->kv_full[t][1], v_it & 1, abort_flag,
+                     p.timeout_ns) &&
+           warp_wait(&bars->p_full[t], (s_cnt - 1) & 1, abort_flag,
+                     p.timeout_ns);
+      if (ok && e == 0)
+        ok = warp_wait(&bars->o_free[t], (ui & 1) ^ 1, abort_flag,
+                       p.timeout_ns);
+      if (!ok) {
+        fail(5);
+        break;
+      }
+      ++v_it;
+      if (leader) {
+        dt_trace<TRACE>(p, bars, kRoleMma, kEvPReady, t, e, mt.unit);
+        tc_fence_after();
+        if (SCORE == BSM_SCORE_SOFTMAX) {
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(o_acc, s_acc + kk * 8, dv + kk * (16 * 128 / 16), idesc_o,
+                   (kk > 0 || e > 0) ? 1u : 0u);
+        } else {
+#pragma unroll 2
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint32_t col = (kk >> 2) * 64 + (kk & 3) * 8;
+            mma_ts(o_acc, s_acc + col, dv + kk * (16 * 128 / 16), idesc_o,
+                   (kk > 0 || e > 0) ? 1u : 0u);
+            mma_ts(o_acc, s_acc + col + 32, dv + kk * (16 * 128 / 16), idesc_o,
+                   1u);
+          }
+        }
+        mma_commit(&bars->pv_done[t]);
+        dt_trace<TRACE>(p, bars, kRoleMma, kEvPVIssued, t, e, mt.unit);
+      }
+      __syncwarp();
+      if (e + 1 < n) {
+        ok = warp_wait(&bars->kv_full[t][0], k_it & 1, abort_flag,
+                       p.timeout_ns);
+        if (!ok) {
+          fail(2);
+          break;
+        }
+        ++k_it;
+        if (leader) {
+          tc_fence_after();
+          issue_s();
+          dt_trace<TRACE>(p, bars, kRoleMma, kEvSIssued, t, e + 1, mt.unit);
+          if (e + 1 == n - 1) mma_commit(&bars->q_empty[t]);
+          mma_commit(&bars->kv_empty[t][0]);
+        }
+        ++s_cnt;
+      }
+      if (leader) mma_commit(&bars->kv_empty[t][1]);
+      __syncwarp();
+    }
+    if (!ok) break;
+    if (leader) mbar_arrive(&bars->list_free[t][buf]);
+    __syncwarp();
+  }
+  if (leader) {
+    mma_commit(&bars->mma_done[t]);
+    if (!mbar_wait_drain(&bars->mma_done[t], 0, p.timeout_ns) && ok)
+      record_timeout(kRoleMma, 6);
+  }
+  __syncwarp();
+}
+
+template <int SCORE, bool KEEP, bool TRACE>
+__device__ __forceinline__ void dt_score_role(const FwdParams& p, DtBars* bars,
+                                              const uint16_t* lists,
+                                              uint32_t tmem, const int t) {
+  constexpr int D = 128;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4;  // TMEM lane quarter this warp may access
+  const int r = quarter * 32 + lane;
+  const bool tracer = (r == 0);
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t s_addr = tmem + lane_off + t * 128;
+  const uint32_t o_addr = tmem + lane_off + 256 + t * 128;
+  volatile int* abort_flag = &bars->abort;
+  const float NEG_INF = __int_as_float(0xff800000);
+  const bool seg = (p.flags & BSM_MASK_SEGMENT) != 0;
+  const bool seg_elem = KEEP && seg && (*p.seg_flags & 1) != 0;
+  const bool dense = KEEP && p.dense != nullptr;
+  uint32_t s_cnt = 0, pv_cnt = 0;
+  for (int ui = 0;; ++ui) {
+    const int buf = ui % kListBufs;
+    if (!warp_wait(&bars->list_full[t][buf], (ui / kListBufs) & 1, abort_flag,
+                   p.timeout_ns)) {
+      record_timeout(kRoleScore, 0);
+      break;
+    }
+    const int unit = bars->meta[t][buf].unit;
+    if (unit < 0) break;
+    const int n_ent = bars->meta[t][buf].n;
+    const UnitCoord uc{bars->meta[t][buf].b, bars->meta[t][buf].h, 0};
+    const uint16_t* list = lists + buf * kMaxKvTiles;
+    const int qrow = bars->meta[t][buf].qt * kTileM + r;
+    const bool row_ok = qrow < p.Sq;
+    // visible keys of this row form [rlo, rhi] (plus the element compare of
+    // unsorted segment ids)
+    int rlo = 0, rhi = p.Skv - 1;
+    if (p.flags & BSM_MASK_CAUSAL) rhi = min(rhi, qrow);
+    if (p.flags & BSM_MASK_LOCAL) rlo = max(rlo, qrow - p.window + 1);
+    if (p.flags & BSM_MASK_BAND) rhi = min(rhi, qrow + p.window - 1);
+    int segq = 0;
+    if (seg && row_ok) {
+      const int64_t qi = static_cast<int64_t>(uc.b) * p.Sq + qrow;
+      if (seg_elem) {
+        segq = p.q_seg[qi];
+      } else {
+        const int2 sr = reinterpret_cast<const int2*>(p.seg_range)[qi];
+        rlo = max(rlo, sr.x);
+        rhi = min(rhi, sr.y);
+      }
+    }
+    const int32_t* segk_b =
+        seg_elem ? p.kv_seg + static_cast<int64_t>(uc.b) * p.Skv : nullptr;
+    float m_used = NEG_INF, l_sum = 0.f;
+    uint32_t unit_pv = 0;
+    bool ok = true;
+    for (int e = 0; e < n_ent; ++e) {
+      const uint32_t ent = list[e];
+      const int cls = static_cast<int>(ent & 3u);
+      if (!cls) continue;
+      const int jt = static_cast<int>(ent >> 2);
+      const int kbase = jt * kTileN;
+      uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (KEEP && cls == 1) {
+        if (seg_elem)
+          segment_bits(keep, segk_b + kbase, min(kTileN, p.Skv - kbase), segq);
+        if (dense) {  // the row's mask words for these 128 keys
+          const int64_t w0 = kbase >> 5;
+          const uint32_t* dw =
+              p.dense + static_cast<int64_t>(row_ok ? qrow : 0) * p.dense_words;
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            keep[w] &= (row_ok && w0 + w < p.dense_words) ? __ldg(dw + w0 + w)
+                                                          : 0u;
+        }
+      }
+      ok = warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, p.timeout_ns);
+      if (!ok) {
+        record_timeout(kRoleScore, 1);
+        break;
+      }
+      ++s_cnt;
+      if (tracer) dt_trace<TRACE>(p, bars, kRoleScore, kEvSFull, t, e, unit);
+      tc_fence_after();
+      uint32_t sraw[kTileN];
+#pragma unroll
+      for (int q = 0; q < kTileN / 32; ++q)
+        tmem_ld32(s_addr + q * 32, sraw + q * 32);
+      tmem_ld_wait();
+      float* s = reinterpret_cast<float*>(sraw);
+      if (cls == 1) mask_tile(s, rlo - kbase, rhi - kbase, keep, KEEP);
+
+      uint32_t pk[16];
+      if (SCORE == BSM_SCORE_SOFTMAX) {
+        // row max: three-input max, four independent chains
+        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+        float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+#pragma unroll
+        for (int c = 8; c < kTileN; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+        }
+        const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3));
+        const float m_blk = mx * p.scale_log2;
+        bool rescale = false;
+        float alpha = 1.f;
+        if (m_blk > m_used + kRescaleLog2) {
+          if (m_used != NEG_INF) {
+            alpha = ex2_approx(m_used - m_blk);
+            rescale = true;
+          }
+          l_sum *= alpha;
+          m_used = m_blk;
+        }
+        const float neg_m = (m_used == NEG_INF) ? 0.f : -m_used;
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kTileN / 32; ++q) {  // 32 columns at a time
+#pragma unroll
+          for (int c = 32 * q; c < 32 * q + 32; c += 4) {
+            // paired f32 FMA/add: the same roundings as one element at a time
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, s[c], s[c + 1], p.scale_log2, neg_m);
+            ffma2(x2, x3, s[c + 2], s[c + 3], p.scale_log2, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(ls0, ls1, ls0, ls1, p0, p1);
+            fadd2(ls2, ls3, ls2, ls3, p2, p3);
+            pk[(c & 31) / 2] = pack_bf16x2(p0, p1);
+            pk[(c & 31) / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(s_addr + q * 16, pk);
+        }
+        l_sum += (ls0 + ls1) + (ls2 + ls3);
+        // Rescale O_t (needs the previous PV of this tile to have landed).
+        if (__any_sync(0xffffffffu, rescale) && unit_pv > 0) {
+          ok = warp_wait(&bars->pv_done[t], (pv_cnt - 1) & 1, abort_flag,
+                         p.timeout_ns);
+          if (!ok) {
+            record_timeout(kRoleScore, 2);
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + q * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(o_addr + q * 32, o);
+          }
+        }
+      } else {
+        // pointwise: x = scale*qk; p = x*sigmoid(x)/Sq; masked (-inf) -> 0.
+        // With sigmoid(x) = (1 + tanh(x/2)) / 2 this is g + g*tanh(x/2),
+        // g = x / (2 Sq): one tanh per element, the rest on paired f32.
+        // hstu_ops multiplies the f32 scores by f32 v, so p is kept to about
+        // 16 bits: p = hi + lo, both bf16 (lo = p - hi is exact in f32).
+        // Each 64-key half's hi and lo (32 columns each) go back over that
+        // half's own 64 columns of S; the MMA warp adds both products into O.
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t pl[16];
+#pragma unroll
+            for (int c = 64 * hf + 32 * q; c < 64 * hf + 32 * q + 32; c += 2) {
+              float h0, h1, g0, g1, p0, p1;
+              fmul2(h0, h1, s[c], s[c + 1], p.pw_half);
+              fmul2(g0, g1, s[c], s[c + 1], p.pw_g);
+              ffma2v(p0, p1, g0, g1, tanh_approx(h0), tanh_approx(h1), g0,
+                     g1);
+              p0 = s[c] != NEG_INF ? p0 : 0.f;
+              p1 = s[c + 1] != NEG_INF ? p1 : 0.f;
+              const uint32_t hi = pack_bf16x2(p0, p1);
+              pk[(c & 31) / 2] = hi;
+              pl[(c & 31) / 2] =
+                  pack_bf16x2(p0 - __uint_as_float(hi << 16),
+                              p1 - __uint_as_float(hi & 0xffff0000u));
+            }
+            tmem_st16(s_addr + hf * 64 + q * 16, pk);
+            tmem_st16(s_addr + hf * 64 + 32 + q * 16, pl);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+      if (tracer) dt_trace<TRACE>(p, bars, kRoleScore, kEvPFull, t, e, unit);
+      ++pv_cnt;
+      ++unit_pv;
+    }
+    if (!ok) break;
+
+    // ---- epilogue: out = O / l (softmax) or O (pointwise), bf16
+    if (tracer) dt_trace<TRACE>(p, bars, kRoleScore, kEvEpiBegin, t, 0, unit);
+    uint16_t* orow = p.out + static_cast<int64_t>(uc.b) * p.o_sb +
+                     static_cast<int64_t>(uc.h) * p.o_sh +
+                     static_cast<int64_t>(qrow) * p.o_ss;
+    if (unit_pv > 0) {
+      if (!warp_wait(&bars->pv_done[t], (pv_cnt - 1) & 1, abort_flag,
+                     p.timeout_ns)) {
+        record_timeout(kRoleScore, 3);
+        break;
+      }
+      tc_fence_after();
+      // all of O_t into registers with one wait; the next unit's first P.V
+      // may then overwrite it while the stores go out
+      uint32_t o[D];
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) tmem_ld32(o_addr + q * 32, o + q * 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      float inv = 1.f;
+      if (SCORE == BSM_SCORE_SOFTMAX) inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      if (row_ok) {
+        // 32 bytes per store where the row alignment allows: each warp
+        // store touches 32 rows, so fewer, wider stores cost fewer requests
+        const bool v8 = p.o_vec8 != 0;
+#pragma unroll
+        for (int v = 0; v < D / 16; ++v) {
+          uint32_t w[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            w[c] = pack_bf16x2(__uint_as_float(o[16 * v + 2 * c]) * inv,
+                               __uint_as_float(o[16 * v + 2 * c + 1]) * inv);
+          if (v8) {
+            st_global_v8(orow + v * 16, w);
+          } else {
+            st_global_v4(orow + v * 16, w[0], w[1], w[2], w[3]);
+            st_global_v4(orow + v * 16 + 8, w[4], w[5], w[6], w[7]);
+          }
+        }
+      }
+    } else {
+      if (row_ok) {
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v)
+          st_global_v4(orow + v * 8, 0u, 0u, 0u, 0u);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+    }
+    if (SCORE == BSM_SCORE_SOFTMAX && p.lse != nullptr && row_ok) {
+      const float lse = l_sum > 0.f
+                            ? (m_used + log2f(l_sum)) * 0.6931471805599453f
+                            : NEG_INF;
+      p.lse[(static_cast<int64_t>(uc.b) * p.H + uc.h) * p.Sq + qrow] = lse;
+    }
+    mbar_arrive(&bars->list_free[t][buf]);
+    if (tracer) dt_trace<TRACE>(p, bars, kRoleScore, kEvEpiEnd, t, 0, unit);
+  }
+}
+
+
+template <int SCORE, bool TRACE>
+__global__ void __launch_bounds__(kDtThreads, 1)
+    splash_fwd_dt_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  DtBars* bars = reinterpret_cast<DtBars*>(smem + kDtOffBar);
+  // the CTA's lists: kListBufs per pipeline
+  uint16_t* lists = p.lists + static_cast<size_t>(blockIdx.x) * 2 * kListBufs *
+                                  kMaxKvTiles;
+  const int warp = threadIdx.x / 32;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      for (int i = 0; i < kListBufs; ++i) {
+        mbar_init(&bars->list_full[t][i], 1);
+        mbar_init(&bars->list_free[t][i], 2 + kTileM);  // load, MMA, score
+      }
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&bars->kv_full[t][s], 1);
+        mbar_init(&bars->kv_empty[t][s], 1);
+      }
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kTileM);
+      mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->o_free[t], kTileM);
+      mbar_init(&bars->mma_done[t], 1);
+    }
+    bars->abort = 0;
+    for (int i = 0; i < 6; ++i) bars->trace_n[i] = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLight>();
+    const int t = warp & 1;
+    uint16_t* lt = lists + t * kListBufs * kMaxKvTiles;
+    if (warp < 2)
+      dt_load_role<TRACE>(p, &tm_q, &tm_k, &tm_v, smem, bars, lt, t);
+    else
+      dt_mma_role<SCORE, TRACE>(p, smem, bars, tmem, t);
+  } else {
+    setmaxnreg_inc<kRegsScore>();
+    const int t = (warp - 4) / 4;
+    const uint16_t* lt = lists + t * kListBufs * kMaxKvTiles;
+    // per-element keep bits only when segment ids are unsorted or an
+    // arbitrary mask is given (read once; the same for every thread)
+    if (((p.flags & BSM_MASK_SEGMENT) && (*p.seg_flags & 1) != 0) ||
+        p.dense != nullptr)
+      dt_score_role<SCORE, true, TRACE>(p, bars, lt, tmem, t);
+    else
+      dt_score_role<SCORE, false, TRACE>(p, bars, lt, tmem, t);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+  if (TRACE && threadIdx.x == 0) {
+    uint32_t* hdr = reinterpret_cast<uint32_t*>(
+        reinterpret_cast<TraceRec*>(p.trace) +
+        static_cast<size_t>(blockIdx.x) * (p.trace_cap + 2));
+    const uint32_t per = p.trace_cap / 6;
+    for (int i = 0; i < 8; ++i) hdr[i] = i < 6 ? min(bars->trace_n[i], per) : 0;
+  }
+}
+
+template <int SCORE>
+cudaError_t launch_dt(const FwdParams& p, const CUtensorMap& tq,
+                      const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                      cudaStream_t stream) {
+  // the instance that records the event trace is launched only with one
+  auto kern = p.trace != nullptr ? splash_fwd_dt_kernel<SCORE, true>
+                                 : splash_fwd_dt_kernel<SCORE, false>;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kDtThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kDtSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDtThreads, kDtSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
 template <int D, int SCORE, bool PINGPONG>
 cudaError_t launch_one(const FwdParams& p, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv,
@@ -1066,6 +1775,13 @@ cudaError_t launch_splash_fwd(const FwdParams& p, const CUtensorMap& tq,
   // is built without it.
   const bool pp = (p.flags & BSM_MASK_SEGMENT) == 0 && p.Skv >= 4096 &&
                   p.dense == nullptr && p.D == 128;
+  // Packed sequences (segment ids, no arbitrary mask) at head dim 128 take
+  // the kernel with decoupled query tiles.
+  const bool dt = (p.flags & BSM_MASK_SEGMENT) != 0 && p.dense == nullptr &&
+                  p.D == 128;
+  if (dt)
+    return pw ? launch_dt<BSM_SCORE_POINTWISE>(p, tq, tk, tv, grid, stream)
+              : launch_dt<BSM_SCORE_SOFTMAX>(p, tq, tk, tv, grid, stream);
   if (p.D == 128) {
     if (pw)
       return pp ? launch_one<128, BSM_SCORE_POINTWISE, true>(p, tq, tk, tv, grid, stream)

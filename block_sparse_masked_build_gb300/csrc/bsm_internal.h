@@ -18,14 +18,16 @@ constexpr int kTileN = 128;
 constexpr int kUnitRows = 2 * kTileM;
 constexpr int kMaxSeq = 262144;
 constexpr int kMaxKvTiles = kMaxSeq / kTileN;  // list capacity per unit
-// Forward workspace: 256 bytes of counters, then per CTA three unit lists of
-// kMaxKvTiles uint16 entries (up to kMaxCtas CTAs).
+// Forward workspace: 256 bytes of counters, then per CTA two sets (one per
+// query-tile pipeline of the packed-sequence kernel; the other kernel uses
+// the first) of three unit lists of kMaxKvTiles uint16 entries (up to
+// kMaxCtas CTAs).
 constexpr int kMaxCtas = 256;
 constexpr int kMaxSuperOrder = 8192;  // longest-first table size limit
 constexpr int kListBufs = 3;
 constexpr size_t kListBytes = static_cast<size_t>(kMaxKvTiles) * 2;
 constexpr size_t kFwdWorkspaceBytes =
-    256 + static_cast<size_t>(kMaxCtas) * kListBufs * kListBytes;
+    256 + static_cast<size_t>(kMaxCtas) * 2 * kListBufs * kListBytes;
 
 struct MaskInfoParams {
   uint32_t flags;

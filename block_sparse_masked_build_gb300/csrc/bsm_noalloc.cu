@@ -7,11 +7,11 @@
 // which the implicit device synchronisation of cudaMalloc is not acceptable.
 // bsm_splash_fwd needs a caller-provided workspace; this variant uses a
 // workspace that lives in the library itself instead: a file-scope device
-// array of bsm::kFwdWorkspaceBytes (3 MiB).
+// array of bsm::kFwdWorkspaceBytes (6 MiB).
 //
 // The array is part of this file's device code.  CUDA loads a library's
 // device code into a context lazily by default (on the first use of one of
-// its kernels or symbols), and that load is when the array's 3 MiB are
+// its kernels or symbols), and that load is when the array's 6 MiB are
 // taken.  So the first call on a device -- which looks the array up -- may
 // take device memory and synchronise; every later call in the same context
 // takes none.  Callers that reserve all free memory make one call first.
@@ -128,7 +128,7 @@ extern "C" bsm_status bsm_splash_fwd_noalloc(
   if (Sq > bsm::kMaxSeq || Skv > bsm::kMaxSeq) {
     bsm::set_last_error(
         "bsm_splash_fwd_noalloc: sequence length above 262144 does not fit "
-        "the library's 3 MiB scratch");
+        "the library's 6 MiB scratch");
     return BSM_ERR_UNSUPPORTED;
   }
   void* scratch = nullptr;

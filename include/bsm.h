@@ -210,7 +210,7 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
                           void* workspace, size_t workspace_bytes,
                           void* stream);
 
-/* Bytes of the forward's device workspace (about 3 MiB): the work-unit
+/* Bytes of the forward's device workspace (about 6 MiB): the work-unit
  * counter and each CTA's lists of the KV tiles of its next units.  The
  * counter is zeroed on `stream` before each launch; the launch overwrites
  * the rest.  Two forward calls that may run at the same time need separate
@@ -223,7 +223,7 @@ size_t bsm_splash_fwd_workspace_bytes(void);
  * reserve all free HBM up front, and loops that cannot afford cudaMalloc's
  * implicit synchronisation can call it: it takes the same arguments as
  * bsm_splash_fwd minus the workspace and allocates nothing (no cudaMalloc,
- * no cudaFree, no allocating library routine).  Its workspace is a 3 MiB
+ * no cudaFree, no allocating library routine).  Its workspace is a 6 MiB
  * (bsm_splash_fwd_workspace_bytes()) array in the library's own device
  * code, held on a device from the moment that code is loaded there until
  * the process exits.

@@ -134,7 +134,7 @@ def test_build_mask_info_argument_errors(lib):
 
 def _fwd(lib, info, B=1, H=2, Hkv=2, Sq=256, Skv=256, D=128, score=0,
          lse=None, seg=(None, None), strides=None, q=0x10000, ws=0x70000,
-         wsb=256 + 256 * 3 * 2048 * 2):
+         wsb=256 + 256 * 2 * 3 * 2048 * 2):
     st = strides or (H * Sq * D, Sq * D, D)
     s3 = I64x3(*st)
     kv3 = I64x3(Hkv * Skv * D, Skv * D, D)
@@ -173,7 +173,7 @@ def test_splash_fwd_argument_errors(lib):
     assert _fwd(lib, info, ws=None) == INVALID
     assert _fwd(lib, info, wsb=8) == INVALID
     assert "workspace" in _lib.last_error()
-    assert lib.bsm_splash_fwd_workspace_bytes() == 256 + 256 * 3 * 2048 * 2
+    assert lib.bsm_splash_fwd_workspace_bytes() == 256 + 256 * 2 * 3 * 2048 * 2
     # an arbitrary-mask info must carry its bits, with full rows
     dense = _info(flags=16)
     assert _fwd(lib, dense) == INVALID
