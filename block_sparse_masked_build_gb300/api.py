@@ -392,6 +392,87 @@ def splash_attention_bwd(q, k, v, out, lse, dout, *,
     return dq, dk, dv
 
 
+_copy_streams: dict = {}
+
+
+def _can_pipeline(q, k, v, out, lse, stream, mask_info, dense_mask):
+    """Host inputs take the chunked path when they (and given outputs) are
+    pinned and contiguous and no prebuilt mask info or arbitrary mask is
+    involved."""
+    ts = [q, k, v] + [t for t in (out, lse) if t is not None]
+    return (all(t.is_pinned() and t.is_contiguous() for t in ts)
+            and mask_info is None and dense_mask is None
+            and (stream is None or isinstance(stream, torch.cuda.Stream))
+            and k.shape[1] > 0 and q.shape[1] % k.shape[1] == 0)
+
+
+def _splash_host_pipelined(q, k, v, flags, window, q_seg, kv_seg, scale,
+                           score, block_q, block_kv, want_lse, out, lse,
+                           stream, dev):
+    """Pinned host inputs, in chunks of heads: the host->device copies of
+    chunk c + 1 (one stream), the forward of chunk c (the call's stream)
+    and the device->host copies of chunk c - 1 (a third stream) overlap.
+    Every copy is a contiguous slab ([b, head range] of a [B, H, S, D]
+    tensor); the mask info is built once, the heads share it."""
+    B, H, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    g = H // Hkv
+    comp = torch.cuda.current_stream(dev) if stream is None else stream
+    if dev not in _copy_streams:
+        _copy_streams[dev] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    cin, cout = _copy_streams[dev]
+    with torch.cuda.stream(comp):
+        qd = torch.empty((B, H, Sq, D), dtype=q.dtype, device=dev)
+        kd = torch.empty((B, Hkv, Skv, D), dtype=k.dtype, device=dev)
+        vd = torch.empty((B, Hkv, Skv, D), dtype=v.dtype, device=dev)
+        od = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=dev)
+        qs = None if q_seg is None else q_seg.to(dev, non_blocking=True)
+        ks = None if kv_seg is None else kv_seg.to(dev, non_blocking=True)
+        info = build_mask_info(flags, B, Sq, Skv, block_q, block_kv, window,
+                               qs, ks, device=dev, stream=comp)
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16,
+                          pin_memory=True)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, pin_memory=True)
+    # K/V head ranges of the chunks (query heads follow their group)
+    n_chunks = min(Hkv, 4)
+    bounds = [Hkv * c // n_chunks for c in range(n_chunks + 1)]
+    for t in (qd, kd, vd):
+        t.record_stream(cin)
+    od.record_stream(cout)
+    cin.wait_stream(comp)
+    for c in range(n_chunks):
+        a, b = bounds[c], bounds[c + 1]
+        qa, qb = a * g, b * g
+        with torch.cuda.stream(cin):
+            for bb in range(B):
+                qd[bb, qa:qb].copy_(q[bb, qa:qb], non_blocking=True)
+                kd[bb, a:b].copy_(k[bb, a:b], non_blocking=True)
+                vd[bb, a:b].copy_(v[bb, a:b], non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(cin)
+        comp.wait_event(loaded)
+        with torch.cuda.stream(comp):
+            lc = (torch.empty((B, qb - qa, Sq), dtype=torch.float32,
+                              device=dev) if want_lse else None)
+            bsm_splash_fwd(qd[:, qa:qb], kd[:, a:b], vd[:, a:b], info, qs, ks,
+                           scale, score, od[:, qa:qb], lc, comp)
+            done = torch.cuda.Event()
+            done.record(comp)
+        if lc is not None:
+            lc.record_stream(cout)
+        with torch.cuda.stream(cout):
+            cout.wait_event(done)
+            for bb in range(B):
+                out[bb, qa:qb].copy_(od[bb, qa:qb], non_blocking=True)
+                if lc is not None:
+                    lse[bb, qa:qb].copy_(lc[bb], non_blocking=True)
+    comp.wait_stream(cout)
+    comp.synchronize()
+    return out, (lse if want_lse else None)
+
+
 def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
                      window: int = 0, q_segment_ids=None, kv_segment_ids=None,
                      scale: float | None = None, score: int = SCORE_SOFTMAX,
@@ -419,6 +500,11 @@ def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
     dev = torch.device("cuda", torch.cuda.current_device()) if host \
         else q.device
     want_lse = return_lse and score == SCORE_SOFTMAX
+    if host and _can_pipeline(q, k, v, out, lse, stream, mask_info,
+                              dense_mask):
+        return _splash_host_pipelined(
+            q, k, v, mask_flags, window, q_segment_ids, kv_segment_ids,
+            scale, score, block_q, block_kv, want_lse, out, lse, stream, dev)
     if host:
         nb = q.is_pinned()
         qd = q.to(dev, non_blocking=nb)

@@ -434,3 +434,40 @@ def test_maximum_sequence_length_local_window():
     got_lse = np.array([lse[b, h, r].item() for b, h, r in rows])
     compare_out(got, ref, what="max-length out")
     compare_lse(got_lse, ref_lse, what="max-length lse")
+
+
+@pytest.mark.parametrize("case", ["causal", "segments", "gqa", "pointwise"])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_inputs_match_device_path(case, pinned):
+    """splash_attention with host tensors (copies in chunks of heads that
+    overlap the forward when the inputs are pinned) returns exactly what
+    the same call on device tensors returns."""
+    B, H, Hkv, S, D = 2, 8, 8, 1024, 128
+    flags, score, seg = C, SM, None
+    if case == "segments":
+        flags = C | SG
+        seg = torch.from_numpy(wl.random_segment_ids(B, S, 40, 500, 5))
+    if case == "gqa":
+        Hkv = 2
+    if case == "pointwise":
+        score = PW
+    q, k, v = _qkv(B, H, Hkv, S, S, D, 606)
+    dev = torch.device("cuda")
+    segd = None if seg is None else seg.to(dev)
+    ref_out, ref_lse = bsm.splash_attention(
+        q.to(dev), k.to(dev), v.to(dev), mask_flags=flags,
+        q_segment_ids=segd, kv_segment_ids=segd, score=score)
+    torch.cuda.synchronize()
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        seg = None if seg is None else seg.pin_memory()
+    out, lse = bsm.splash_attention(q, k, v, mask_flags=flags,
+                                    q_segment_ids=seg, kv_segment_ids=seg,
+                                    score=score)
+    assert out.device.type == "cpu"
+    assert torch.equal(out, ref_out.cpu())
+    if score == SM:
+        assert torch.equal(lse, ref_lse.cpu())
+    else:
+        assert lse is None and ref_lse is None
+    assert bsm.bsm_device_status()[0] == 0
