@@ -1,4 +1,7 @@
-// Block-sparse masked attention forward for sm_103a (GB300).
+// Block-sparse masked attention forward for sm_103a (GB300).  Two kernels:
+// the lockstep one described here, and, for packed sequences (segment ids)
+// at head dim 128, a variant whose two query tiles run as independent
+// pipelines (see "Decoupled query tiles" below).
 //
 // One persistent CTA per SM takes work units of (batch, head, 256 query
 // rows) from a counter in the caller's workspace, longest units first.  A
