@@ -554,7 +554,12 @@ def forward_roofline(w, flops, fwd_ms, peaks, traffic):
     peak HBM B/s), else HBM-bound and reported in GB/s."""
     nbytes = algorithmic_bytes(w)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    common = {"kernel": "splash_fwd_kernel", "traffic": traffic,
+    # segment-id masks (no arbitrary mask) at head dim 128 run the kernel
+    # with decoupled query tiles
+    dt = (w.flags & wl.MASK_SEGMENT) and not (w.flags & wl.MASK_DENSE) \
+        and w.D == 128
+    common = {"kernel": "splash_fwd_dt_kernel" if dt else "splash_fwd_kernel",
+              "traffic": traffic,
               "algorithmic_bytes": nbytes,
               "flop_per_byte": round(flops / nbytes, 1),
               "ridge_flop_per_byte": round(ridge, 1),
