@@ -25,7 +25,8 @@
 //
 // Warp roles (320 threads): warp 0 loads with TMA (the CTA's fixed pair of
 // tiles once, then the streamed pair of every step through a two-stage
-// ring), warp 1 issues the tcgen05 MMAs (lane 0) and owns the TMEM
+// ring), warp 1 issues the tcgen05 MMAs (the whole warp runs the issuing
+// code, the lane elect.sync picks sends each MMA) and owns the TMEM
 // allocation, warps 2-9 do the elementwise work, a thread per TMEM lane (a
 // row of the fixed tiles) and column half.  Per step, with F0/F1 the fixed tiles and
 // T0/T1 the streamed ones (dK/dV: F = K, V and T = Q, dO; dQ: F = Q, dO and
@@ -316,19 +317,19 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
-      mma_ss(t_s, da + off, t0 + off, idesc_s, k > 0 ? 1u : 0u);
+      mma_ss_elect(t_s, da + off, t0 + off, idesc_s, k > 0 ? 1u : 0u);
     }
-    mma_commit(&bars->s_full);
+    mma_commit_elect(&bars->s_full);
   };
   auto issue_dp = [&](int it) {
     const uint64_t t1 = db + (it & 1) * 2 * kTileUnits + kTileUnits;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (kTileM * 128 / 16) + (k & 3) * 2;
-      mma_ss(t_dp, da + kTileUnits + off, t1 + off, idesc_s,
-             k > 0 ? 1u : 0u);
+      mma_ss_elect(t_dp, da + kTileUnits + off, t1 + off, idesc_s,
+                   k > 0 ? 1u : 0u);
     }
-    mma_commit(&bars->dp_full);
+    mma_commit_elect(&bars->dp_full);
   };
   // Per step: once P is stored (dK/dV) or S has been read (dQ), dV += P T1
   // and the next step's S go in; once dS is stored, dK += dS T0 (dQ += dS
@@ -341,12 +342,11 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
   if (ok && n_iter > 0) {
     ok = bwarp_wait(&bars->t_full[0], 0, abort_flag, p.timeout_ns);
     if (!ok && leader) record_bwd_timeout(kRoleBMma, 1);
-    if (ok && leader) {
+    if (ok) {
       tc_fence_after();
       issue_s(0);
       issue_dp(0);
     }
-    __syncwarp();
   }
   for (int it = 0; ok && it < n_iter; ++it) {
     const int s = it & 1;
@@ -358,18 +358,15 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
       if (leader) record_bwd_timeout(kRoleBMma, 2);
       break;
     }
-    if (leader) {
-      tc_fence_after();
-      // bf16 A from TMEM: rows 16kk..16kk+15 of the K dimension in columns
-      // 8kk..8kk+7
-      if (DKDV) {
+    tc_fence_after();
+    // bf16 A from TMEM: rows 16kk..16kk+15 of the K dimension in columns
+    // 8kk..8kk+7
+    if (DKDV) {
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // dV += P T1
-          mma_ts(t_acc0, t_s + kk * 8, m1 + kk * (16 * 128 / 16), idesc_acc,
-                 (kk > 0 || first) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kTileN / 16; ++kk)  // dV += P T1
+        mma_ts_elect(t_acc0, t_s + kk * 8, m1 + kk * (16 * 128 / 16),
+                     idesc_acc, (kk > 0 || first) ? 1u : 0u);
     }
-    __syncwarp();
     const bool more = it + 1 < n_iter;
     if (more) {
       ok = bwarp_wait(&bars->t_full[(it + 1) & 1], ((it + 1) >> 1) & 1,
@@ -378,35 +375,28 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, uint8_t* smem,
         if (leader) record_bwd_timeout(kRoleBMma, 1);
         break;
       }
-      if (leader) {
-        tc_fence_after();
-        issue_s(it + 1);
-      }
-      __syncwarp();
+      tc_fence_after();
+      issue_s(it + 1);
     }
     ok = bwarp_wait(&bars->ds_ready, it & 1, abort_flag, p.timeout_ns);
     if (!ok) {
       if (leader) record_bwd_timeout(kRoleBMma, 4);
       break;
     }
-    if (leader) {
-      tc_fence_after();
+    tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kTileN / 16; ++kk)  // dK (or dQ) += dS T0
-        mma_ts(DKDV ? t_acc1 : t_acc0, t_dp + kk * 8,
-               m0 + kk * (16 * 128 / 16), idesc_acc,
-               (kk > 0 || first) ? 1u : 0u);
-      mma_commit(&bars->t_empty[s]);
-      if (more) issue_dp(it + 1);
-    }
-    __syncwarp();
+    for (int kk = 0; kk < kTileN / 16; ++kk)  // dK (or dQ) += dS T0
+      mma_ts_elect(DKDV ? t_acc1 : t_acc0, t_dp + kk * 8,
+                   m0 + kk * (16 * 128 / 16), idesc_acc,
+                   (kk > 0 || first) ? 1u : 0u);
+    mma_commit_elect(&bars->t_empty[s]);
+    if (more) issue_dp(it + 1);
   }
-  if (leader) {
-    mma_commit(&bars->acc_done);
-    mma_commit(&bars->mma_done);
-    if (!mbar_wait_drain(&bars->mma_done, 0, p.timeout_ns) && ok)
-      record_bwd_timeout(kRoleBMma, 3);
-  }
+  __syncwarp();
+  mma_commit_elect(&bars->acc_done);
+  mma_commit_elect(&bars->mma_done);
+  if (leader && !mbar_wait_drain(&bars->mma_done, 0, p.timeout_ns) && ok)
+    record_bwd_timeout(kRoleBMma, 3);
   __syncwarp();
 }
 
