@@ -57,7 +57,7 @@ constexpr int kThreads = 384;
 // thread, the two score warpgroups rise to kRegsScore.  Their sum must stay
 // within what the CTA was launched with (kThreads x the kernel's register
 // count), which the launcher checks.
-constexpr uint32_t kRegsLight = 72, kRegsScore = 208;
+constexpr uint32_t kRegsLight = 80, kRegsScore = 208;
 constexpr int kRegsNeeded = 128 * kRegsLight + 256 * kRegsScore;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kPingPongMin = 12;  // see score_role
