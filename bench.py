@@ -554,10 +554,10 @@ def forward_roofline(w, flops, fwd_ms, peaks, traffic):
     peak HBM B/s), else HBM-bound and reported in GB/s."""
     nbytes = algorithmic_bytes(w)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    # segment-id masks (no arbitrary mask) at head dim 128 run the kernel
-    # with decoupled query tiles
-    dt = (w.flags & wl.MASK_SEGMENT) and not (w.flags & wl.MASK_DENSE) \
-        and w.D == 128
+    # at head dim 128 without an arbitrary mask, segment-id masks and masks
+    # of fewer than 4096 keys run the kernel with decoupled query tiles
+    dt = not (w.flags & wl.MASK_DENSE) and w.D == 128 and \
+        ((w.flags & wl.MASK_SEGMENT) or w.Skv_ < 4096)
     common = {"kernel": "splash_fwd_dt_kernel" if dt else "splash_fwd_kernel",
               "traffic": traffic,
               "algorithmic_bytes": nbytes,
