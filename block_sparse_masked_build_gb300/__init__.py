@@ -24,6 +24,8 @@ from .api import (  # noqa: F401
     bsm_splash_bwd,
     bsm_splash_bwd_workspace_bytes,
     bsm_splash_fwd,
+    bsm_splash_fwd_host,
+    bsm_splash_fwd_host_bytes,
     bsm_splash_fwd_workspace_bytes,
     bsm_version,
     build_mask_info,

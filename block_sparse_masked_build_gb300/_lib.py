@@ -29,7 +29,7 @@ STATUS_NAMES = {
 }
 
 
-ABI_VERSION = 301  # the struct layouts below
+ABI_VERSION = 302  # the struct layouts below
 
 
 class MaskSpec(ctypes.Structure):
@@ -92,6 +92,16 @@ def _declare(lib):
         c.POINTER(MaskInfoStruct), c.c_void_p, c.c_void_p, c.c_float,
         c.c_int32, c.c_void_p, c.c_void_p, c.c_void_p, c.c_size_t,
         c.c_void_p]
+    lib.bsm_splash_fwd_host_bytes.restype = c.c_size_t
+    lib.bsm_splash_fwd_host_bytes.argtypes = [
+        c.POINTER(MaskSpec), c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+        c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32]
+    lib.bsm_splash_fwd_host.restype = c.c_int
+    lib.bsm_splash_fwd_host.argtypes = [
+        c.POINTER(MaskSpec), c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
+        c.c_void_p, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+        c.c_int32, c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_void_p,
+        c.c_void_p, c.c_void_p, c.c_size_t, c.c_int32, c.c_void_p]
     lib.bsm_splash_fwd_noalloc.restype = c.c_int
     lib.bsm_splash_fwd_noalloc.argtypes = [
         c.c_void_p, c.c_void_p, c.c_void_p, I64x3, I64x3, I64x3, I64x3,

@@ -209,6 +209,35 @@ def bsm_splash_fwd(q, k, v, mask_info: MaskInfo, q_segment_ids,
         workspace.numel() * workspace.element_size(), sh))
 
 
+def bsm_splash_fwd_host_bytes(flags: int, window: int, B: int, H: int,
+                              H_kv: int, Sq: int, Skv: int, D: int,
+                              block_q: int, block_kv: int, score: int) -> int:
+    spec = MaskSpec(flags, window)
+    return int(_lib.lib().bsm_splash_fwd_host_bytes(
+        ctypes.byref(spec), B, H, H_kv, Sq, Skv, D, block_q, block_kv, score))
+
+
+def bsm_splash_fwd_host(flags: int, window: int, q, k, v, q_segment_ids,
+                        kv_segment_ids, block_q: int, block_kv: int,
+                        scale: float, score: int, out, lse, device_buffer,
+                        n_chunks: int = 0, stream=None) -> None:
+    """The forward on contiguous CPU tensors (pinned for overlap): q
+    [B,H,Sq,D], k/v [B,H_kv,Skv,D] bf16, segment ids int32 [B,S], out
+    [B,H,Sq,D] bf16 and lse [B,H,Sq] f32 (or None); device_buffer a CUDA
+    uint8 tensor of bsm_splash_fwd_host_bytes(...) bytes.  Enqueued on
+    `stream`; out and lse are ready once it is synchronised."""
+    B, H, Sq, D = q.shape
+    H_kv, Skv = k.shape[1], k.shape[2]
+    spec = MaskSpec(flags, window)
+    _check(_lib.lib().bsm_splash_fwd_host(
+        ctypes.byref(spec), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+        _ptr(q_segment_ids), _ptr(kv_segment_ids), B, H, H_kv, Sq, Skv, D,
+        block_q, block_kv, float(scale), int(score), out.data_ptr(),
+        _ptr(lse), device_buffer.data_ptr(),
+        device_buffer.numel() * device_buffer.element_size(), int(n_chunks),
+        _stream_handle(stream)))
+
+
 def bsm_splash_fwd_noalloc(q, k, v, mask_info: MaskInfo, q_segment_ids,
                            kv_segment_ids, scale: float, score: int, out,
                            lse=None, stream=None) -> None:
@@ -392,15 +421,14 @@ def splash_attention_bwd(q, k, v, out, lse, dout, *,
     return dq, dk, dv
 
 
-_copy_streams: dict = {}
-
-
-def _can_pipeline(q, k, v, out, lse, stream, mask_info, dense_mask):
-    """Host inputs take the chunked path when they (and given outputs) are
-    pinned and contiguous and no prebuilt mask info or arbitrary mask is
-    involved."""
-    ts = [q, k, v] + [t for t in (out, lse) if t is not None]
-    return (all(t.is_pinned() and t.is_contiguous() for t in ts)
+def _can_pipeline(q, k, v, out, lse, q_seg, kv_seg, stream, mask_info,
+                  dense_mask):
+    """Host inputs go through bsm_splash_fwd_host (chunked copies that
+    overlap the forward when the memory is pinned) when they and any given
+    outputs are contiguous CPU tensors, and no prebuilt mask info or
+    arbitrary mask is involved."""
+    ts = [q, k, v] + [t for t in (out, lse, q_seg, kv_seg) if t is not None]
+    return (all(t.device.type == "cpu" and t.is_contiguous() for t in ts)
             and mask_info is None and dense_mask is None
             and (stream is None or isinstance(stream, torch.cuda.Stream))
             and k.shape[1] > 0 and q.shape[1] % k.shape[1] == 0)
@@ -409,66 +437,29 @@ def _can_pipeline(q, k, v, out, lse, stream, mask_info, dense_mask):
 def _splash_host_pipelined(q, k, v, flags, window, q_seg, kv_seg, scale,
                            score, block_q, block_kv, want_lse, out, lse,
                            stream, dev):
-    """Pinned host inputs, in chunks of heads: the host->device copies of
-    chunk c + 1 (one stream), the forward of chunk c (the call's stream)
-    and the device->host copies of chunk c - 1 (a third stream) overlap.
-    Every copy is a contiguous slab ([b, head range] of a [B, H, S, D]
-    tensor); the mask info is built once, the heads share it."""
+    """Host tensors through bsm_splash_fwd_host: one call that copies in,
+    builds the mask info, runs the forward and copies out, pipelined over
+    ranges of heads on the library's copy streams."""
     B, H, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
-    g = H // Hkv
     comp = torch.cuda.current_stream(dev) if stream is None else stream
-    if dev not in _copy_streams:
-        _copy_streams[dev] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
-    cin, cout = _copy_streams[dev]
+    nbytes = bsm_splash_fwd_host_bytes(flags, window, B, H, Hkv, Sq, Skv, D,
+                                       block_q, block_kv, score)
+    if nbytes == 0:
+        raise BsmError(_lib.BSM_ERR_INVALID_ARG,
+                       "bsm_splash_fwd_host_bytes: bad arguments")
     with torch.cuda.stream(comp):
-        qd = torch.empty((B, H, Sq, D), dtype=q.dtype, device=dev)
-        kd = torch.empty((B, Hkv, Skv, D), dtype=k.dtype, device=dev)
-        vd = torch.empty((B, Hkv, Skv, D), dtype=v.dtype, device=dev)
-        od = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=dev)
-        qs = None if q_seg is None else q_seg.to(dev, non_blocking=True)
-        ks = None if kv_seg is None else kv_seg.to(dev, non_blocking=True)
-        info = build_mask_info(flags, B, Sq, Skv, block_q, block_kv, window,
-                               qs, ks, device=dev, stream=comp)
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     if out is None:
         out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16,
                           pin_memory=True)
     if want_lse and lse is None:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, pin_memory=True)
-    # K/V head ranges of the chunks (query heads follow their group)
-    n_chunks = min(Hkv, 4)
-    bounds = [Hkv * c // n_chunks for c in range(n_chunks + 1)]
-    for t in (qd, kd, vd):
-        t.record_stream(cin)
-    od.record_stream(cout)
-    cin.wait_stream(comp)
-    for c in range(n_chunks):
-        a, b = bounds[c], bounds[c + 1]
-        qa, qb = a * g, b * g
-        with torch.cuda.stream(cin):
-            for bb in range(B):
-                qd[bb, qa:qb].copy_(q[bb, qa:qb], non_blocking=True)
-                kd[bb, a:b].copy_(k[bb, a:b], non_blocking=True)
-                vd[bb, a:b].copy_(v[bb, a:b], non_blocking=True)
-            loaded = torch.cuda.Event()
-            loaded.record(cin)
-        comp.wait_event(loaded)
-        with torch.cuda.stream(comp):
-            lc = (torch.empty((B, qb - qa, Sq), dtype=torch.float32,
-                              device=dev) if want_lse else None)
-            bsm_splash_fwd(qd[:, qa:qb], kd[:, a:b], vd[:, a:b], info, qs, ks,
-                           scale, score, od[:, qa:qb], lc, comp)
-            done = torch.cuda.Event()
-            done.record(comp)
-        if lc is not None:
-            lc.record_stream(cout)
-        with torch.cuda.stream(cout):
-            cout.wait_event(done)
-            for bb in range(B):
-                out[bb, qa:qb].copy_(od[bb, qa:qb], non_blocking=True)
-                if lc is not None:
-                    lse[bb, qa:qb].copy_(lc[bb], non_blocking=True)
-    comp.wait_stream(cout)
+    qs = None if q_seg is None else q_seg.to(torch.int32).contiguous()
+    ks = None if kv_seg is None else kv_seg.to(torch.int32).contiguous()
+    bsm_splash_fwd_host(flags, window, q, k, v, qs, ks, block_q, block_kv,
+                        scale, score, out, lse if want_lse else None, buf,
+                        0, comp)
     comp.synchronize()
     return out, (lse if want_lse else None)
 
@@ -500,8 +491,8 @@ def splash_attention(q, k, v, *, mask_flags: int = MASK_CAUSAL,
     dev = torch.device("cuda", torch.cuda.current_device()) if host \
         else q.device
     want_lse = return_lse and score == SCORE_SOFTMAX
-    if host and _can_pipeline(q, k, v, out, lse, stream, mask_info,
-                              dense_mask):
+    if host and _can_pipeline(q, k, v, out, lse, q_segment_ids,
+                              kv_segment_ids, stream, mask_info, dense_mask):
         return _splash_host_pipelined(
             q, k, v, mask_flags, window, q_segment_ids, kv_segment_ids,
             scale, score, block_q, block_kv, want_lse, out, lse, stream, dev)

@@ -727,6 +727,6 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq) {
 
 const char* bsm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t bsm_version(void) { return 301; }
+int32_t bsm_version(void) { return 302; }
 
 }  // extern "C"

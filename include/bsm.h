@@ -217,6 +217,52 @@ bsm_status bsm_splash_fwd(const void* q, const void* k, const void* v,
  * workspaces. */
 size_t bsm_splash_fwd_workspace_bytes(void);
 
+/* Bytes of the device buffer bsm_splash_fwd_host needs (0 on bad
+ * arguments): device copies of q, k, v, out, lse (SOFTMAX) and the segment
+ * ids (SEGMENT), the mask info and the forward's workspace. */
+size_t bsm_splash_fwd_host_bytes(const bsm_mask_spec* spec, int32_t B,
+                                 int32_t H, int32_t H_kv, int32_t Sq,
+                                 int32_t Skv, int32_t D, int32_t block_q,
+                                 int32_t block_kv, int32_t score);
+
+/* The forward on host buffers, end to end (this entry point has no
+ * counterpart in the pages; it is a property of this library): copies the
+ * inputs to the device, builds the mask info, runs bsm_splash_fwd and
+ * copies out (and lse) back, pipelined over n_chunks ranges of K/V heads
+ * (their query heads follow): the host-to-device copies of one range, the
+ * forward of the previous one and the device-to-host copies of the one
+ * before that run at the same time, on two copy streams the library keeps
+ * per device (made on the first call in a CUDA context) and the caller's
+ * stream.  Each range moves as one strided copy per tensor.
+ *   spec, block_q, block_kv, scale, score  as for bsm_build_mask_info and
+ *               bsm_splash_fwd (spec->dense_bits, if any, is device memory)
+ *   q           host bf16 [B][H][Sq][D], contiguous
+ *   k, v        host bf16 [B][H_kv][Skv][D], contiguous
+ *   q/kv_segment_ids  host int32 [B][Sq] / [B][Skv]; both iff SEGMENT
+ *   out         host bf16 [B][H][Sq][D]; lse host f32 [B][H][Sq] or NULL
+ *               (NULL for POINTWISE)
+ *   device_buffer  device, >= bsm_splash_fwd_host_bytes(...) bytes,
+ *               256-byte aligned, owned by the caller; two calls that may
+ *               run at the same time need separate buffers
+ *   n_chunks    1..16 head ranges, capped at H_kv; <= 0 picks 8
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * copies from or to pageable memory are correct but do not overlap.
+ * Everything is enqueued: the call returns once the work is issued and
+ * `stream` waits for the last copy, so out and lse are ready after the
+ * stream is synchronised.  Argument errors as for bsm_splash_fwd, found
+ * before anything is enqueued; a CUDA error part-way returns BSM_ERR_CUDA
+ * with the work enqueued until then left to run. */
+bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
+                               const void* k, const void* v,
+                               const int32_t* q_segment_ids,
+                               const int32_t* kv_segment_ids, int32_t B,
+                               int32_t H, int32_t H_kv, int32_t Sq,
+                               int32_t Skv, int32_t D, int32_t block_q,
+                               int32_t block_kv, float scale, int32_t score,
+                               void* out, float* lse, void* device_buffer,
+                               size_t device_bytes, int32_t n_chunks,
+                               void* stream);
+
 /* bsm_splash_fwd for callers that cannot allocate device memory (this entry
  * point has no counterpart in the pages; it is a property of this library).
  * Plugins handed finished buffers by a host framework, serving engines that
@@ -333,8 +379,9 @@ int32_t bsm_debug_fwd_grid(int32_t B, int32_t H, int32_t Sq);
 /* Thread-local text of the last error of this thread ("" if none). */
 const char* bsm_last_error(void);
 
-/* ABI version (major*10000 + minor*100 + patch): 301 = 0.3.1, adding
- * bsm_pack_dense_mask to 0.3.0 (the backward entry points and bsm_tensor
+/* ABI version (major*10000 + minor*100 + patch): 302 = 0.3.2, adding
+ * bsm_splash_fwd_host and bsm_splash_fwd_host_bytes to 0.3.1 (which added
+ * bsm_pack_dense_mask to 0.3.0: the backward entry points and bsm_tensor
  * added to 0.2.0's forward, mask spec and mask info). */
 int32_t bsm_version(void);
 

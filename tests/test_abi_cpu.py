@@ -42,7 +42,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.bsm_version() == 301 == _lib.ABI_VERSION
+    assert lib.bsm_version() == 302 == _lib.ABI_VERSION
 
 
 def test_library_is_built_for_sm_103a(lib):
@@ -226,3 +226,66 @@ def test_bwd_workspace_bytes(lib):
     assert lib.bsm_splash_bwd_workspace_bytes(1, 3, 100, 0) == 1280
     assert lib.bsm_splash_bwd_workspace_bytes(2, 16, 8192, 1) == 0
     assert lib.bsm_splash_bwd_workspace_bytes(-1, 16, 8192, 0) == 0
+
+
+def test_host_entry_buffer_bytes(lib):
+    # device copies of q, k, v, out, lse and the segment ids, the mask info
+    # and the forward's workspace, each 256-aligned
+    spec = MaskSpec(5, 0)
+    B, H, Hkv, S, D = 2, 16, 4, 8192, 128
+    mi = lib.bsm_mask_info_bytes(ctypes.byref(spec), B, S, S, 128, 128)
+    ws = lib.bsm_splash_fwd_workspace_bytes()
+    qo, kv = B * H * S * D * 2, B * Hkv * S * D * 2
+    want = (2 * _align(qo) + 2 * _align(kv) + _align(B * H * S * 4)
+            + 2 * _align(B * S * 4) + _align(mi) + _align(ws))
+    got = lib.bsm_splash_fwd_host_bytes(ctypes.byref(spec), B, H, Hkv, S, S,
+                                        D, 128, 128, 0)
+    assert got == want
+    # pointwise: no lse; no segment ids without SEGMENT
+    causal = MaskSpec(1, 0)
+    mi1 = lib.bsm_mask_info_bytes(ctypes.byref(causal), B, S, S, 128, 128)
+    got = lib.bsm_splash_fwd_host_bytes(ctypes.byref(causal), B, H, Hkv, S,
+                                        S, D, 128, 128, 1)
+    assert got == 2 * _align(qo) + 2 * _align(kv) + _align(mi1) + _align(ws)
+    # bad block size or negative size
+    assert lib.bsm_splash_fwd_host_bytes(ctypes.byref(spec), B, H, Hkv, S, S,
+                                         D, 100, 128, 0) == 0
+    assert lib.bsm_splash_fwd_host_bytes(ctypes.byref(spec), -1, H, Hkv, S,
+                                         S, D, 128, 128, 0) == 0
+
+
+def _host(lib, flags=1, B=2, H=4, Hkv=4, S=256, D=128, score=0, q=0x10000,
+          seg=(None, None), lse=0x30000, buf=0x100000, nbuf=None):
+    spec = MaskSpec(flags, 0)
+    if nbuf is None:
+        nbuf = lib.bsm_splash_fwd_host_bytes(ctypes.byref(spec), max(B, 0),
+                                             max(H, 0), max(Hkv, 1), max(S, 0),
+                                             max(S, 0), 128, 128, 128, score)
+    return lib.bsm_splash_fwd_host(
+        ctypes.byref(spec), q, 0x20000, 0x20000, seg[0], seg[1], B, H, Hkv, S,
+        S, D, 128, 128, 0.1, score, 0x40000, lse, buf, nbuf, 0, None)
+
+
+def test_host_entry_argument_errors(lib):
+    # every check below is made before anything touches the device
+    assert _host(lib, D=96) == UNSUPPORTED
+    assert "head_dim" in _lib.last_error()
+    assert _host(lib, H=3, Hkv=2) == INVALID
+    assert _host(lib, score=1) == INVALID               # pointwise with lse
+    assert "logsumexp" in _lib.last_error()
+    assert _host(lib, score=5) == INVALID
+    assert _host(lib, flags=5) == INVALID               # SEGMENT, no ids
+    assert _host(lib, seg=(0x50000, 0x60000)) == INVALID  # ids, no SEGMENT
+    assert _host(lib, flags=5, seg=(0x50000, None)) == INVALID
+    assert "segment" in _lib.last_error()
+    assert _host(lib, q=None) == INVALID
+    assert _host(lib, buf=None) == INVALID
+    assert _host(lib, buf=0x100010) == INVALID           # not 256-aligned
+    assert _host(lib, nbuf=1024) == INVALID
+    assert "device buffer" in _lib.last_error()
+    assert _host(lib, B=-1) == INVALID
+
+
+def test_host_entry_empty_input_is_a_no_op(lib):
+    assert _host(lib, B=0, q=None, lse=None) == 0
+    assert _host(lib, S=0, q=None, lse=None) == 0

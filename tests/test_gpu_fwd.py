@@ -436,12 +436,50 @@ def test_maximum_sequence_length_local_window():
     compare_lse(got_lse, ref_lse, what="max-length lse")
 
 
+@pytest.mark.parametrize("n_chunks", [1, 3, 16])
+def test_host_entry_chunks_match_device_path(n_chunks):
+    """bsm_splash_fwd_host over ragged head ranges (5 K/V heads in 1, 3 or
+    5 ranges; grouped query heads, packed segments, a ragged sequence
+    length) returns exactly the device path's out and lse, also when two
+    calls run back to back on one device buffer with other inputs."""
+    B, H, Hkv, S, D = 2, 10, 5, 1000, 128
+    flags = C | SG
+    dev = torch.device("cuda")
+    outs = []
+    nbytes = bsm.bsm_splash_fwd_host_bytes(flags, 0, B, H, Hkv, S, S, D, 128,
+                                           128, SM)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    cases = []
+    for seed in (707, 708):
+        q, k, v = (t.pin_memory() for t in _qkv(B, H, Hkv, S, S, D, seed))
+        seg = torch.from_numpy(wl.random_segment_ids(B, S, 30, 400, seed))
+        seg = seg.pin_memory()
+        out = torch.empty((B, H, S, D), dtype=torch.bfloat16).pin_memory()
+        lse = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+        cases.append((q, k, v, seg, out, lse))
+    stream = torch.cuda.current_stream()
+    for q, k, v, seg, out, lse in cases:   # both enqueued before a sync
+        bsm.bsm_splash_fwd_host(flags, 0, q, k, v, seg, seg, 128, 128,
+                                1.0 / math.sqrt(D), SM, out, lse, buf,
+                                n_chunks, stream)
+    stream.synchronize()
+    assert bsm.bsm_device_status()[0] == 0
+    for q, k, v, seg, out, lse in cases:
+        segd = seg.to(dev)
+        ref_out, ref_lse = bsm.splash_attention(
+            q.to(dev), k.to(dev), v.to(dev), mask_flags=flags,
+            q_segment_ids=segd, kv_segment_ids=segd)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out.cpu())
+        assert torch.equal(lse, ref_lse.cpu())
+
+
 @pytest.mark.parametrize("case", ["causal", "segments", "gqa", "pointwise"])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_inputs_match_device_path(case, pinned):
-    """splash_attention with host tensors (copies in chunks of heads that
-    overlap the forward when the inputs are pinned) returns exactly what
-    the same call on device tensors returns."""
+    """splash_attention with host tensors (bsm_splash_fwd_host: copies in
+    chunks of heads that overlap the forward when the memory is pinned)
+    returns exactly what the same call on device tensors returns."""
     B, H, Hkv, S, D = 2, 8, 8, 1024, 128
     flags, score, seg = C, SM, None
     if case == "segments":
