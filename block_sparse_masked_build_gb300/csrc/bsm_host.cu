@@ -25,7 +25,7 @@
 namespace {
 
 constexpr int kMaxHostChunks = 16;
-constexpr int kDefaultHostChunks = 8;
+constexpr int kDefaultHostChunks = 4;
 constexpr int kMaxDevices = 64;
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }

@@ -244,7 +244,7 @@ size_t bsm_splash_fwd_host_bytes(const bsm_mask_spec* spec, int32_t B,
  *   device_buffer  device, >= bsm_splash_fwd_host_bytes(...) bytes,
  *               256-byte aligned, owned by the caller; two calls that may
  *               run at the same time need separate buffers
- *   n_chunks    1..16 head ranges, capped at H_kv; <= 0 picks 8
+ *   n_chunks    1..16 head ranges, capped at H_kv; <= 0 picks 4
  * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister):
  * copies from or to pageable memory are correct but do not overlap.
  * Everything is enqueued: the call returns once the work is issued and
