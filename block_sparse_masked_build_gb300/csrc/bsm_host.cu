@@ -279,6 +279,15 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
   if (e == cudaSuccess) e = cudaStreamWaitEvent(r->in, r->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(r->out, r->start, 0);
   if (e != cudaSuccess) return cuda_error(e, "stream fork");
+  // After a failure part-way the caller's stream still waits for the
+  // copies already enqueued, so the device buffer is free once it is
+  // synchronised (best effort: the failure may be the stream's own).
+  auto join_fail = [&](bsm_status status) {
+    for (cudaStream_t c : {r->in, r->out})
+      if (cudaEventRecord(r->finish, c) == cudaSuccess)
+        cudaStreamWaitEvent(s, r->finish, 0);
+    return status;
+  };
 
   // segment ids in and the mask info, on the caller's stream
   if (seg) {
@@ -288,12 +297,12 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
       e = cudaMemcpyAsync(ksd, kv_segment_ids,
                           static_cast<size_t>(B) * Skv * 4,
                           cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_error(e, "segment ids");
+    if (e != cudaSuccess) return join_fail(cuda_error(e, "segment ids"));
   }
   bsm_mask_info info;
   st = bsm_build_mask_info(spec, qsd, ksd, B, Sq, Skv, block_q, block_kv,
                            base + L.mi, L.ws - L.mi, &info, stream);
-  if (st != BSM_OK) return st;
+  if (st != BSM_OK) return join_fail(st);
 
   const int64_t q_strides[3] = {static_cast<int64_t>(H) * Sq * D,
                                 static_cast<int64_t>(Sq) * D, D};
@@ -314,7 +323,8 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
                     nkv * kv_head, B, cudaMemcpyHostToDevice, r->in);
     if (e == cudaSuccess) e = cudaEventRecord(r->loaded[c], r->in);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, r->loaded[c], 0);
-    if (e != cudaSuccess) return cuda_error(e, "host-to-device copies");
+    if (e != cudaSuccess)
+      return join_fail(cuda_error(e, "host-to-device copies"));
     // the chunk's forward; its lse goes to [B][nq][Sq] at B * qa * Sq
     float* lse_c = lsed ? lsed + static_cast<size_t>(B) * qa * Sq : nullptr;
     st = bsm_splash_fwd(qd + qa * q_head, kd + a * kv_head, vd + a * kv_head,
@@ -322,7 +332,7 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
                         nkv, Sq, Skv, D, &info, qsd, ksd, scale, score,
                         od + qa * q_head, lse_c, base + L.ws,
                         bsm::kFwdWorkspaceBytes, stream);
-    if (st != BSM_OK) return st;
+    if (st != BSM_OK) return join_fail(st);
     e = cudaEventRecord(r->done[c], s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(r->out, r->done[c], 0);
     // out: the chunk's rows of out and lse
@@ -335,7 +345,8 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
                     static_cast<size_t>(nq) * Sq * 4,
                     static_cast<size_t>(nq) * Sq * 4, B,
                     cudaMemcpyDeviceToHost, r->out);
-    if (e != cudaSuccess) return cuda_error(e, "device-to-host copies");
+    if (e != cudaSuccess)
+      return join_fail(cuda_error(e, "device-to-host copies"));
   }
   // the caller's stream ends after the last copy out; the copy-in stream
   // has nothing left after the last chunk's forward waited for it

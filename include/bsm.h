@@ -250,8 +250,9 @@ size_t bsm_splash_fwd_host_bytes(const bsm_mask_spec* spec, int32_t B,
  * Everything is enqueued: the call returns once the work is issued and
  * `stream` waits for the last copy, so out and lse are ready after the
  * stream is synchronised.  Argument errors as for bsm_splash_fwd, found
- * before anything is enqueued; a CUDA error part-way returns BSM_ERR_CUDA
- * with the work enqueued until then left to run. */
+ * before anything is enqueued; a failure part-way returns its status with
+ * the work enqueued until then left to run, `stream` still waiting for it
+ * (so the device buffer is free once `stream` is synchronised). */
 bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
                                const void* k, const void* v,
                                const int32_t* q_segment_ids,
