@@ -1,7 +1,8 @@
 // Block-sparse masked attention forward for sm_103a (GB300).  Two kernels:
-// the lockstep one described here, and, for packed sequences (segment ids)
-// at head dim 128, a variant whose two query tiles run as independent
-// pipelines (see "Decoupled query tiles" below).
+// the lockstep one described here, and, at head dim 128 for packed
+// sequences (segment ids) and for any mask below 4096 keys, a variant whose
+// two query tiles run as independent pipelines (see "Decoupled query
+// tiles" below).
 //
 // One persistent CTA per SM takes work units of (batch, head, 256 query
 // rows) from a counter in the caller's workspace, longest units first.  A
@@ -18,7 +19,8 @@
 //   warp 0      issues TMA loads: Q per query tile, K and V tiles through a
 //               ring of shared-memory slots (128-byte swizzle).
 //   warps 1,2   one MMA issuer per query tile (warp 1 also allocates the 512
-//               TMEM columns): the warp waits, one lane issues tcgen05 MMAs
+//               TMEM columns): the whole warp waits and issues, each
+//               tcgen05 MMA going out from the lane elect.sync picks:
 //               S_t = Q_t K^T (both operands in shared memory) and
 //               O_t += P_t V (P_t read from TMEM, V from shared memory).
 //   warps 4-7   score warpgroup of query tile 0, warps 8-11 of tile 1: one
@@ -1021,7 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // units (one query tile of one (batch, head)), builds its own KV-tile list,
 // and has its own Q buffer and two-slot K/V ring, so one pipeline's unit
 // boundary overlaps the other's work on the tensor core.  K/V tiles are not
-// shared between the tiles (L2 carries the reuse).
+// shared between the tiles (L2 carries the reuse).  Masks without segment
+// ids take this kernel too below 4096 keys, where units are short as well.
 //
 // Warp roles (384 threads, three warpgroups, registers split as above):
 // warps 0/1 take pipeline 0/1's units, build their lists and load their
