@@ -659,6 +659,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     b = g / gridDim.y;
   }
   const int table = (p.flags & BSM_MASK_SEGMENT) ? b : 0;
+  // The dQ grid reads nothing the dK/dV grid writes, so it is launched as
+  // its programmatic dependent: once every dK/dV CTA has started, dQ CTAs
+  // take the SMs the dK/dV grid's last CTAs leave.
+  if (DKDV && threadIdx.x == 0)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->f_full, 1);
@@ -710,6 +715,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kBwdTmemCols);
+  // a dQ grid ends only after the dK/dV grid it overlapped, so work queued
+  // after the backward on the stream sees both
+  if (!DKDV && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // D_q = sum_d dO[q, d] * out[q, d]: D / 8 threads per (batch, head, row),
@@ -763,8 +772,24 @@ cudaError_t launch_bwd_one(const BwdParams& p, const CUtensorMap& tq,
   if (e != cudaSuccess) return e;
   const dim3 grid = DKDV ? dim3((p.Skv + kTileN - 1) / kTileN, p.Hkv, p.B)
                          : dim3((p.Sq + kTileM - 1) / kTileM, p.H, p.B);
-  kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
-  return cudaGetLastError();
+  if (DKDV) {
+    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+  }
+  // dQ: a programmatic dependent of the launch before it (the dK/dV grid,
+  // which lets it start early; or D_q's, which does not, so dQ then starts
+  // after it as usual)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p);
 }
 
 template <int D, int SCORE>
