@@ -177,3 +177,35 @@ def test_flop_counts_of_every_workload_are_positive():
             continue  # the long local-window count takes longer; pinned elsewhere
         f = bench.workload_flops(w, wl.make_segment_ids(w))
         assert f > 0, name
+
+
+def test_recorded_traffic_lines_are_well_formed():
+    # every TRAFFIC_JSON line of the ncu summaries names a bench workload and
+    # a per-launch DRAM figure within a plausible multiple of that
+    # workload's algorithmic bytes; the roofline takes a line only when its
+    # source hash is the current forward sources' hash
+    sys.path.insert(0, ROOT)
+    import json
+    import re
+    import bench
+    from block_sparse_masked_build_gb300 import workloads as wl
+
+    prof = os.path.join(ROOT, "profiles")
+    seen = 0
+    for name in sorted(os.listdir(prof)):
+        with open(os.path.join(prof, name)) as f:
+            for line in f:
+                m = re.match(r"\s*TRAFFIC_JSON:\s*(\{.*\})\s*$", line)
+                if not m:
+                    continue
+                d = json.loads(m.group(1))
+                assert set(d) == {"src", "workload", "dram_bytes_per_launch"}
+                assert re.fullmatch(r"[0-9a-f]{16}", d["src"])
+                w = wl.WORKLOADS[d["workload"]]
+                algo = bench.algorithmic_bytes(w)
+                assert 0.5 * algo < d["dram_bytes_per_launch"] < 5 * algo
+                got = bench.recorded_traffic(d["workload"])
+                if d["src"] == bench.fwd_source_hash():
+                    assert got == float(d["dram_bytes_per_launch"])
+                seen += 1
+    assert seen >= 1
