@@ -155,14 +155,25 @@ bsm_status copy_resources(CopyRes** out) {
   return BSM_OK;
 }
 
-// Rows [0, rows) of `width` bytes, at `dpitch` / `spitch` byte strides.
+// Rows [0, rows) of `width` bytes, at `dpitch` / `spitch` byte strides:
+// one strided copy, or one copy per row where a pitch is above what a
+// strided copy takes (`max_pitch`, the device's cudaDevAttrMaxPitch).
 cudaError_t copy_rows(void* dst, size_t dpitch, const void* src,
                       size_t spitch, size_t width, size_t rows,
-                      cudaMemcpyKind kind, cudaStream_t s) {
+                      size_t max_pitch, cudaMemcpyKind kind,
+                      cudaStream_t s) {
   if (width == 0 || rows == 0) return cudaSuccess;
   if (rows == 1 || (dpitch == width && spitch == width))
     return cudaMemcpyAsync(dst, src, width * rows, kind, s);
-  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+  if (dpitch <= max_pitch && spitch <= max_pitch)
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+  for (size_t r = 0; r < rows; ++r) {
+    const cudaError_t e = cudaMemcpyAsync(
+        static_cast<uint8_t*>(dst) + r * dpitch,
+        static_cast<const uint8_t*>(src) + r * spitch, width, kind, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -248,6 +259,12 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
   CopyRes* r = nullptr;
   bsm_status st = copy_resources(&r);
   if (st != BSM_OK) return st;
+  int dev = 0, pitch_attr = 0;
+  cudaError_t ae = cudaGetDevice(&dev);
+  if (ae == cudaSuccess)
+    ae = cudaDeviceGetAttribute(&pitch_attr, cudaDevAttrMaxPitch, dev);
+  if (ae != cudaSuccess) return cuda_error(ae, "device attributes");
+  const size_t max_pitch = pitch_attr > 0 ? static_cast<size_t>(pitch_attr) : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(device_buffer);
@@ -314,13 +331,13 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
     const int nkv = b - a, nq = nkv * g, qa = a * g;
     // in: the chunk's heads of every batch row
     e = copy_rows(qd + qa * q_head, q_pitch, qh + qa * q_head, q_pitch,
-                  nq * q_head, B, cudaMemcpyHostToDevice, r->in);
+                  nq * q_head, B, max_pitch, cudaMemcpyHostToDevice, r->in);
     if (e == cudaSuccess)
       e = copy_rows(kd + a * kv_head, kv_pitch, kh + a * kv_head, kv_pitch,
-                    nkv * kv_head, B, cudaMemcpyHostToDevice, r->in);
+                    nkv * kv_head, B, max_pitch, cudaMemcpyHostToDevice, r->in);
     if (e == cudaSuccess)
       e = copy_rows(vd + a * kv_head, kv_pitch, vh + a * kv_head, kv_pitch,
-                    nkv * kv_head, B, cudaMemcpyHostToDevice, r->in);
+                    nkv * kv_head, B, max_pitch, cudaMemcpyHostToDevice, r->in);
     if (e == cudaSuccess) e = cudaEventRecord(r->loaded[c], r->in);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, r->loaded[c], 0);
     if (e != cudaSuccess)
@@ -338,13 +355,13 @@ bsm_status bsm_splash_fwd_host(const bsm_mask_spec* spec, const void* q,
     // out: the chunk's rows of out and lse
     if (e == cudaSuccess)
       e = copy_rows(oh + qa * q_head, q_pitch, od + qa * q_head, q_pitch,
-                    nq * q_head, B, cudaMemcpyDeviceToHost, r->out);
+                    nq * q_head, B, max_pitch, cudaMemcpyDeviceToHost, r->out);
     if (e == cudaSuccess && lse != nullptr)
       e = copy_rows(lse + static_cast<size_t>(qa) * Sq,
                     static_cast<size_t>(H) * Sq * 4, lse_c,
                     static_cast<size_t>(nq) * Sq * 4,
                     static_cast<size_t>(nq) * Sq * 4, B,
-                    cudaMemcpyDeviceToHost, r->out);
+                    max_pitch, cudaMemcpyDeviceToHost, r->out);
     if (e != cudaSuccess)
       return join_fail(cuda_error(e, "device-to-host copies"));
   }
