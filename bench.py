@@ -624,9 +624,13 @@ def run_e2e(args, w, q, k, v, seg, flops, dev):
            + (0 if sh is None else 2 * sh.nbytes)
            + (0 if dh is None else dh.nbytes))
     d2h = oh.nbytes + (0 if lh is None else lh.nbytes)
+    via = ("splash_attention -> bsm_splash_fwd_host (pinned host tensors)"
+           if dh is None else
+           "splash_attention (pinned host tensors; mask packed on the GPU)")
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "steps": args.e2e_steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "call": via}
 
 
 # ----------------------------------------------------- oracle (CPU) arm
